@@ -1,0 +1,67 @@
+"""Checks of the seeded input generator (no GPU)."""
+import numpy as np
+import torch
+
+import workloads as wl
+
+
+def test_e4m3_encode_matches_library_cast():
+    # library reference: torch's fp32 -> float8_e4m3fn cast (round to nearest
+    # even) of values already clamped to the finite range
+    x = np.concatenate([
+        wl.normal_f32(0, 50, 100_000) * 100,
+        wl.normal_f32(0, 51, 50_000) * 0.01,
+        np.array([0.0, -0.0, 448.0, -448.0, 449.0, 500.0, 2 ** -10, 2 ** -9, 3 * 2 ** -10,
+                  1.0625, 1.1875, 2 ** -6 * (1 - 2 ** -5)], np.float32)])
+    x = x.astype(np.float32)
+    got = wl.e4m3_encode(x)
+    ref = torch.from_numpy(np.clip(x, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    bad = np.nonzero(got != ref)[0]
+    assert len(bad) == 0, [(float(x[i]), hex(got[i]), hex(ref[i])) for i in bad[:5]]
+
+
+def test_quantise_recipe():
+    x = wl.normal_f32(0, 1, 4 * 256).reshape(4, 256)
+    q, s = wl.quantize_rows_1x128(x)
+    amax = np.abs(x.reshape(4, 2, 128)).max(axis=2)
+    assert np.array_equal(s, (amax / np.float32(448)).astype(np.float32))
+    deq = torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    # every block reaches +-448 at its maximum and round-trips within half an ulp
+    assert (np.abs(deq.reshape(4, 2, 128)).max(axis=2) == 448).all()
+    rel = np.abs(deq * np.repeat(s, 128, axis=1) - x) / np.maximum(np.abs(x), 1e-30)
+    assert np.median(rel) < 2 ** -4
+
+
+def test_quantise_blocks_ragged_n():
+    x = wl.normal_f32(0, 2, 200 * 256).reshape(200, 256)
+    q, s = wl.quantize_blocks_128x128(x)
+    assert s.shape == (2, 2) and q.shape == (200, 256)
+    assert s[1, 0] == np.float32(np.abs(x[128:, :128]).max() / np.float32(448))
+
+
+def test_zero_block_gets_unit_scale():
+    x = np.zeros((2, 128), np.float32)
+    q, s = wl.quantize_rows_1x128(x)
+    assert (s == 1).all() and (q == 0).all()
+
+
+def test_generator_deterministic_and_sliceable():
+    a = wl.normal_f32(0, 1, 10_000)
+    b = wl.normal_f32(0, 1, 10_000)
+    assert np.array_equal(a, b)
+    c = wl.normal_f32(0, 1, 3000, start=4000)
+    assert np.array_equal(a[4000:7000], c)
+    assert abs(float(a.mean())) < 0.05 and abs(float(a.std()) - 1) < 0.05
+
+
+def test_group_recipes():
+    rows = wl.contiguous_group_rows(8)
+    assert len(rows) == 8 and all(1024 <= r <= 6144 and r % 128 == 0 for r in rows)
+    counts = wl.masked_counts(16, 256)
+    assert len(counts) == 16 and counts.min() >= 0 and counts.max() <= 256
+
+
+def test_problem_accounting():
+    p = wl.make_nt(128, 256, 512)
+    assert p.flops() == 2 * 128 * 256 * 512
+    assert p.algorithmic_bytes() == 264_224
