@@ -1,0 +1,418 @@
+// api.cu -- the C ABI declared in include/fp8gemm.h: argument validation,
+// tile-configuration choice, TMA descriptor encoding and launch.
+//
+// Source of the launch shape: DeepGEMM fp8_gemm.cuh, Gemm::run (a persistent
+// grid of at most one CTA per SM) and the make_2d_tma_*_desc factories (the
+// operand and output layouts).  Unlike the page's launcher, nothing here
+// aborts: every failure is returned as a status code.
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fp8gemm.h"
+#include "launch.h"
+
+namespace {
+
+using fp8g::LaunchArgs;
+using fp8g::Params;
+
+constexpr int kVersion = 10000;          // 1.0.0
+constexpr int kDefaultSms = 152;
+constexpr int kMaxDevices = 64;
+constexpr long long kMaxDim = 1ll << 30;  // rows, N and K limits (int32-safe indexing)
+
+__device__ int g_error_word;              // sticky device-side error bits, per device
+
+std::atomic<int> g_override_bn{0};
+std::atomic<int> g_override_split{0};
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+
+// ------------------------------------------------------------ device facts
+
+struct DeviceInfo {
+    int sms = 0;
+    int *error_word = nullptr;
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+int current_device_info(DeviceInfo &out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return FP8G_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_dev_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (d.sms == 0) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+            return FP8G_ERR_CUDA;
+        void *w = nullptr;
+        if (cudaGetSymbolAddress(&w, g_error_word) != cudaSuccess)
+            return FP8G_ERR_CUDA;
+        d.error_word = static_cast<int *>(w);
+        d.sms = sms;
+    }
+    out = d;
+    return FP8G_OK;
+}
+
+int sms_or_default()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+        return sms;
+    cudaGetLastError();  // clear a "no device" error left by the probe
+    return kDefaultSms;
+}
+
+// ------------------------------------------------------------ tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// A 2-D row-major view: `inner` contiguous elements per row, `outer` rows,
+// `row_bytes` between rows; tiles of box_inner x box_outer elements.
+bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
+              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    std::memset(m, 0, sizeof(*m));
+    return enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ validation
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_common(const void *A, const float *SFA, const void *B, const float *SFB, void *D, long long rows,
+                 int N, int K)
+{
+    if (!A || !SFA || !B || !SFB || !D)
+        return FP8G_ERR_INVALID_ARG;
+    if (rows < 0 || N < 0 || K <= 0)
+        return FP8G_ERR_INVALID_ARG;
+    if (K % 128 != 0 || N % 16 != 0)
+        return FP8G_ERR_UNSUPPORTED;
+    if (rows > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return FP8G_ERR_UNSUPPORTED;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16) || !aligned(SFA, 16) || !aligned(SFB, 4))
+        return FP8G_ERR_MISALIGNED;
+    return FP8G_OK;
+}
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+int pick_block_n(int N, bool many_tiles)
+{
+    const int o = g_override_bn.load();
+    if (o)
+        return o;
+    if (N <= 128)
+        return 128;
+    return many_tiles ? 256 : 128;
+}
+
+size_t split_workspace_bytes(int M, int N, int K, int block_n, int ctas)
+{
+    const long long tiles = (long long)ceil_div(M, 128) * ceil_div(N, block_n);
+    const size_t counters = ((size_t)tiles * 8 * sizeof(int) + 255) / 256 * 256;
+    const size_t partials = (size_t)2 * ctas * 128 * block_n * sizeof(float);
+    (void)K;
+    return counters + partials;
+}
+
+struct NtChoice {
+    int block_n;
+    int split_ctas;   // 0: not split
+    int grid;
+    int tiles;
+};
+
+// Tile shape and schedule for a plain GEMM on a device with `sms` SMs.
+// workspace_bytes < 0 means "as much as it needs".
+int choose_nt(int M, int N, int K, int sms, long long workspace_bytes, NtChoice &c)
+{
+    const int mb = ceil_div(M, 128);
+    const bool many = (long long)mb * ceil_div(N, 256) >= sms;
+    c.block_n = pick_block_n(N, many);
+    c.tiles = mb * ceil_div(N, c.block_n);
+    c.split_ctas = 0;
+    const int kb = K / 128;
+    const int o = g_override_split.load();
+    if (o > 0) {
+        if (c.block_n != 128)
+            return FP8G_ERR_INVALID_ARG;
+        const int P = (int)std::min<long long>(o, (long long)c.tiles * kb);
+        if (workspace_bytes >= 0 && (long long)split_workspace_bytes(M, N, K, 128, P) > workspace_bytes)
+            return FP8G_ERR_WORKSPACE;
+        c.split_ctas = P;
+    } else if (o == 0 && c.block_n == 128 && c.tiles < sms && kb >= 8) {
+        // fewer output tiles than SMs: share the K blocks of all tiles evenly
+        // over the SMs, at least 4 K blocks per CTA
+        const long long P = std::min<long long>(sms, (long long)c.tiles * kb / 4);
+        if (P > c.tiles &&
+            (workspace_bytes < 0 ||
+             (long long)split_workspace_bytes(M, N, K, 128, (int)P) <= workspace_bytes))
+            c.split_ctas = (int)P;
+    }
+    c.grid = c.split_ctas ? c.split_ctas : std::min(sms, c.tiles);
+    return FP8G_OK;
+}
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA; }
+
+void fill_common(Params &p, long long rows, int N, int K, int G, const float *SFA, const float *SFB, void *D,
+                 const int *layout, int block_n, const DeviceInfo &dev)
+{
+    std::memset(&p, 0, sizeof(p));
+    p.rows = (int)rows;
+    p.N = N;
+    p.K = K;
+    p.G = G;
+    p.kb = K / 128;
+    p.nb = ceil_div(N, 128);
+    p.sfa_ld = (int)((rows + 3) / 4 * 4);
+    p.sfa = SFA;
+    p.sfb = SFB;
+    p.layout = layout;
+    p.d = static_cast<__nv_bfloat16 *>(D);
+    p.num_n_blocks = ceil_div(N, block_n);
+    p.error_word = dev.error_word;
+    p.timeout_ns = g_timeout_ns.load();
+}
+
+bool make_maps(LaunchArgs &a, const void *A, const void *B, void *D, long long a_rows, long long b_rows,
+               long long d_rows, int N, int K, int block_n)
+{
+    return make_map(&a.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, a_rows, K, 128, 128,
+                    CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(&a.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, b_rows, K, 128, block_n,
+                    CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(&a.tmap_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, N, d_rows, (uint64_t)N * 2, 32, 32,
+                    CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+}  // namespace
+
+// ============================================================================ C ABI
+
+extern "C" {
+
+int fp8_gemm_nt(const void *A, const float *SFA, const void *B, const float *SFB, void *D, int M, int N, int K,
+                void *workspace, size_t workspace_bytes, fp8g_stream_t stream)
+{
+    int st = check_common(A, SFA, B, SFB, D, M, N, K);
+    if (st != FP8G_OK)
+        return st;
+    if (M == 0 || N == 0)
+        return FP8G_OK;
+    DeviceInfo dev;
+    if ((st = current_device_info(dev)) != FP8G_OK)
+        return st;
+    NtChoice c;
+    const long long ws = workspace ? (long long)workspace_bytes : 0;
+    if ((st = choose_nt(M, N, K, dev.sms, ws, c)) != FP8G_OK)
+        return st;
+    if (c.split_ctas && !aligned(workspace, 256))
+        return FP8G_ERR_MISALIGNED;
+
+    LaunchArgs a;
+    fill_common(a.p, M, N, K, 1, SFA, SFB, D, nullptr, c.block_n, dev);
+    a.p.num_m_blocks = ceil_div(M, 128);
+    a.p.group_m = 8;
+    a.p.num_tiles = c.tiles;
+    if (c.split_ctas) {
+        a.p.units = (long long)c.tiles * a.p.kb;
+        const size_t counters = ((size_t)c.tiles * 8 * sizeof(int) + 255) / 256 * 256;
+        a.p.counters = static_cast<int *>(workspace);
+        a.p.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + counters);
+    }
+    if (!make_maps(a, A, B, D, M, N, M, N, K, c.block_n))
+        return FP8G_ERR_CUDA;
+    a.grid = c.grid;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    return to_status(fp8g::launch_nt(c.block_n, c.split_ctas != 0, a));
+}
+
+int fp8_gemm_grouped_contiguous(const void *A, const float *SFA, const void *B, const float *SFB, void *D,
+                                const int *m_indices, int M_total, int N, int K, int G, void *workspace,
+                                size_t workspace_bytes, fp8g_stream_t stream)
+{
+    (void)workspace;
+    (void)workspace_bytes;
+    int st = check_common(A, SFA, B, SFB, D, M_total, N, K);
+    if (st != FP8G_OK)
+        return st;
+    if (!m_indices || G <= 0)
+        return FP8G_ERR_INVALID_ARG;
+    if (!aligned(m_indices, 4))
+        return FP8G_ERR_MISALIGNED;
+    if (M_total % 128 != 0 || (long long)G * N > kMaxDim)
+        return FP8G_ERR_UNSUPPORTED;
+    if (M_total == 0 || N == 0)
+        return FP8G_OK;
+    DeviceInfo dev;
+    if ((st = current_device_info(dev)) != FP8G_OK)
+        return st;
+    const int mb = M_total / 128;
+    const int block_n = pick_block_n(N, (long long)mb * ceil_div(N, 256) >= dev.sms);
+    LaunchArgs a;
+    fill_common(a.p, M_total, N, K, G, SFA, SFB, D, m_indices, block_n, dev);
+    a.p.num_m_blocks = mb;
+    a.p.group_m = 8;
+    a.p.num_tiles = mb * a.p.num_n_blocks;
+    if (!make_maps(a, A, B, D, M_total, (long long)G * N, M_total, N, K, block_n))
+        return FP8G_ERR_CUDA;
+    a.grid = std::min(dev.sms, a.p.num_tiles);
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    return to_status(fp8g::launch_contiguous(block_n, a));
+}
+
+int fp8_gemm_grouped_masked(const void *A, const float *SFA, const void *B, const float *SFB, void *D,
+                            const int *masked_m, int G, int M_max, int N, int K, void *workspace,
+                            size_t workspace_bytes, fp8g_stream_t stream)
+{
+    (void)workspace;
+    (void)workspace_bytes;
+    int st = check_common(A, SFA, B, SFB, D, M_max, N, K);
+    if (st != FP8G_OK)
+        return st;
+    if (!masked_m || G <= 0)
+        return FP8G_ERR_INVALID_ARG;
+    if (!aligned(masked_m, 4))
+        return FP8G_ERR_MISALIGNED;
+    if ((long long)G * M_max > kMaxDim || (long long)G * N > kMaxDim)
+        return FP8G_ERR_UNSUPPORTED;
+    if (M_max == 0 || N == 0)
+        return FP8G_OK;
+    DeviceInfo dev;
+    if ((st = current_device_info(dev)) != FP8G_OK)
+        return st;
+    const int mb = ceil_div(M_max, 128);
+    const long long tiles_max256 = (long long)G * mb * ceil_div(N, 256);
+    const int block_n = pick_block_n(N, tiles_max256 >= dev.sms);
+    LaunchArgs a;
+    fill_common(a.p, M_max, N, K, G, SFA, SFB, D, masked_m, block_n, dev);
+    a.p.num_m_blocks = mb;
+    a.p.group_m = mb;   // all m-blocks of a (group, n-block) run together: B is read once
+    const long long tiles_max = (long long)G * mb * a.p.num_n_blocks;
+    if (!make_maps(a, A, B, D, (long long)G * M_max, (long long)G * N, (long long)G * M_max, N, K, block_n))
+        return FP8G_ERR_CUDA;
+    a.grid = (int)std::min<long long>(dev.sms, tiles_max);
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    return to_status(fp8g::launch_masked(block_n, a));
+}
+
+size_t fp8_gemm_workspace_size(int kind, int M, int N, int K, int G)
+{
+    (void)G;
+    if (kind != FP8G_KIND_NT || M <= 0 || N <= 0 || K <= 0 || K % 128 != 0)
+        return 0;
+    NtChoice c;
+    if (choose_nt(M, N, K, sms_or_default(), -1, c) != FP8G_OK || !c.split_ctas)
+        return 0;
+    return split_workspace_bytes(M, N, K, 128, c.split_ctas);
+}
+
+size_t fp8_gemm_workspace_size_for(int M, int N, int K, int block_n, int split_ctas)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || split_ctas <= 0 || (block_n != 128 && block_n != 256))
+        return 0;
+    return split_workspace_bytes(M, N, K, block_n, split_ctas);
+}
+
+int fp8_gemm_get_device_error(fp8g_stream_t stream)
+{
+    DeviceInfo dev;
+    int st = current_device_info(dev);
+    if (st != FP8G_OK)
+        return st;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return FP8G_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, dev.error_word, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FP8G_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(dev.error_word, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return FP8G_ERR_CUDA;
+    }
+    if (v & fp8g::kErrTimeoutBit)
+        return FP8G_ERR_TIMEOUT;
+    if (v & fp8g::kErrBadGroupBit)
+        return FP8G_ERR_BAD_GROUP;
+    return FP8G_OK;
+}
+
+const char *fp8_gemm_status_string(int status)
+{
+    switch (status) {
+    case FP8G_OK: return "ok";
+    case FP8G_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or G <= 0)";
+    case FP8G_ERR_UNSUPPORTED: return "unsupported shape (needs K % 128 == 0, N % 16 == 0, M_total % 128 == 0)";
+    case FP8G_ERR_MISALIGNED: return "misaligned pointer (A, B, D, SFA need 16 bytes, SFB 4, workspace 256)";
+    case FP8G_ERR_CUDA: return "a CUDA call failed";
+    case FP8G_ERR_TIMEOUT: return "a pipeline wait on the device ran out of time";
+    case FP8G_ERR_BAD_GROUP: return "a group index or count was out of range";
+    case FP8G_ERR_WORKSPACE: return "workspace too small for the forced split";
+    default: return "unknown status";
+    }
+}
+
+int fp8_gemm_sfa_ld(int M) { return M < 0 ? 0 : (M + 3) / 4 * 4; }
+
+int fp8_gemm_set_override(int block_n, int split_ctas)
+{
+    if (block_n != 0 && block_n != 128 && block_n != 256)
+        return FP8G_ERR_INVALID_ARG;
+    if (split_ctas > 0 && block_n == 256)
+        return FP8G_ERR_INVALID_ARG;
+    g_override_bn.store(block_n);
+    g_override_split.store(split_ctas);
+    return FP8G_OK;
+}
+
+int fp8_gemm_set_wait_timeout_ns(uint64_t ns)
+{
+    if (ns < 1000000ull)
+        return FP8G_ERR_INVALID_ARG;
+    g_timeout_ns.store(ns);
+    return FP8G_OK;
+}
+
+int fp8_gemm_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,31 @@
+// gemm_params.h -- the kernel's by-value argument block (host and device).
+#pragma once
+
+#include <cuda_bf16.h>
+
+namespace fp8g {
+
+// Bits of the sticky device-side error word.
+enum : int { kErrTimeoutBit = 1, kErrBadGroupBit = 2 };
+
+struct Params {
+    int rows;          // NT: M, contiguous: M_total, masked: M_max
+    int N, K, G;
+    int kb, nb;        // K/128, ceil(N/128)
+    int sfa_ld;        // round_up(rows, 4)
+    const float *sfa;
+    const float *sfb;
+    const int *layout; // contiguous: m_indices; masked: masked_m
+    __nv_bfloat16 *d;
+    int num_m_blocks;  // ceil(rows/128) (masked: per group, at most)
+    int num_n_blocks;  // ceil(N/BN)
+    int group_m;       // rasterisation band height, in m-blocks
+    int num_tiles;     // NT and contiguous
+    long long units;   // split: num_tiles * kb
+    float *partials;   // split: 2 * gridDim.x slots of 128 x BN fp32
+    int *counters;     // split: num_tiles * 8 tickets
+    int *error_word;
+    unsigned long long timeout_ns;
+};
+
+}  // namespace fp8g

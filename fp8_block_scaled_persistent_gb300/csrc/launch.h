@@ -1,0 +1,26 @@
+// launch.h -- host-side launch interface between the C ABI (api.cu) and the
+// kernel instantiations (gemm_nt.cu, gemm_contiguous.cu, gemm_masked.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gemm_params.h"
+
+namespace fp8g {
+
+struct LaunchArgs {
+    CUtensorMap tmap_a, tmap_b, tmap_d;
+    Params p;
+    int grid;
+    cudaStream_t stream;
+};
+
+// Dynamic shared memory a launch with tiles of `block_n` columns needs.
+int smem_bytes_for(int block_n);
+
+cudaError_t launch_nt(int block_n, bool split, const LaunchArgs &a);
+cudaError_t launch_contiguous(int block_n, const LaunchArgs &a);
+cudaError_t launch_masked(int block_n, const LaunchArgs &a);
+
+}  // namespace fp8g

@@ -1,0 +1,40 @@
+// launch_impl.cuh -- one launch of a kernel instantiation (persistent grid,
+// 320 threads, the configuration's dynamic shared memory).
+#pragma once
+
+#include <atomic>
+
+#include "gemm_kernel.cuh"
+#include "launch.h"
+
+namespace fp8g {
+
+template <int BN, int KIND, bool SPLIT>
+cudaError_t launch_one(const LaunchArgs &a)
+{
+    auto kern = fp8_gemm_kernel<BN, KIND, SPLIT>;
+    constexpr int smem = Cfg<BN>::kSmemBytes;
+    // The opt-in shared-memory size is a per-device function attribute.
+    static std::atomic<unsigned long long> attr_done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess)
+            return e;
+        attr_done.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.grid, 1, 1);
+    cfg.blockDim = dim3(kNumThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = a.stream;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, kern, a.tmap_a, a.tmap_b, a.tmap_d, a.p);
+}
+
+}  // namespace fp8g

@@ -1,0 +1,172 @@
+/*
+ * fp8gemm.h -- C ABI of the GB300 (sm_103a) FP8 block-scaled GEMM library.
+ *
+ * Operation (all three entry points):
+ *
+ *   D[m][n] = bf16( sum_{k < K/128} SFA[k][m] * SFB[n/128][k] *
+ *                   sum_{t < 128} A[m][128k+t] * B[n][128k+t] )
+ *
+ * A and B hold OCP E4M3FN bytes.  A carries one fp32 scale per row per
+ * 128-wide K block, B one fp32 scale per 128x128 block.  Each 128-K partial
+ * product is accumulated in fp32 and promoted into an fp32 accumulator with
+ * its two scales; D is rounded to bf16 (round to nearest even).
+ * Source: DeepGEMM fp8_gemm.cuh -- fp8_gemm_kernel (per-128-channel scaling
+ * checks, the math warp-groups' promotion of each K block with
+ * scale_a * scale_b, the bf16 epilogue) and the Gemm class's TMA descriptor
+ * factories, which fix the layouts below.
+ *
+ * Layouts (row-major, C order; every pointer is a DEVICE pointer):
+ *   A    e4m3 [M][K]                 masked: [G][M_max][K]
+ *   SFA  fp32 [K/128][sfa_ld(M)]     masked: [G][K/128][sfa_ld(M_max)]
+ *        (M-major: SFA[k][m] scales A[m][128k .. 128k+127]; the leading
+ *        dimension is M rounded up to a multiple of 4, as the Gemm class's
+ *        make_2d_tma_scales_a_desc pads it; pad entries are never read)
+ *   B    e4m3 [G][N][K]              (G = 1 for fp8_gemm_nt; "NT": K is the
+ *        contiguous dimension of both operands)
+ *   SFB  fp32 [G][ceil(N/128)][K/128]
+ *   D    bf16 [M][N]                 masked: [G][M_max][N]
+ *
+ * Requirements (checked on the host before anything is launched):
+ *   K % 128 == 0 and K > 0 (the kernel's BLOCK_K == 128 scaling contract);
+ *   N % 16 == 0 (16-byte rows of D for the tensor-memory-access store);
+ *   A, B, D, SFA 16-byte aligned; SFB 4-byte aligned;
+ *   contiguous: M_total % 128 == 0 (every 128-row block belongs to one group).
+ *
+ * Ownership and synchronisation: the caller owns every buffer.  Calls are
+ * asynchronous on `stream` and allocate nothing.  The host never reads the
+ * device-side group layout (m_indices, masked_m), so no call synchronises.
+ * Calls on different streams may run concurrently if their workspaces differ.
+ *
+ * Errors: every entry point returns an fp8g_status.  Argument errors are
+ * returned synchronously and nothing is launched.  Errors found on the
+ * device (a bounded wait that ran out, a group index out of range) are
+ * recorded in a per-device sticky flag that fp8_gemm_get_device_error
+ * reads and clears.  Nothing aborts, prints or throws.
+ */
+#ifndef FP8GEMM_H
+#define FP8GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st *fp8g_stream_t;
+
+enum fp8g_status {
+    FP8G_OK = 0,
+    FP8G_ERR_INVALID_ARG = 1,  /* null pointer, negative size, G <= 0        */
+    FP8G_ERR_UNSUPPORTED = 2,  /* K % 128, N % 16, M_total % 128, size limits */
+    FP8G_ERR_MISALIGNED = 3,   /* pointer alignment (see Requirements)        */
+    FP8G_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed           */
+    FP8G_ERR_TIMEOUT = 5,      /* device: a bounded pipeline wait ran out     */
+    FP8G_ERR_BAD_GROUP = 6,    /* device: group index / count out of range    */
+    FP8G_ERR_WORKSPACE = 7     /* workspace smaller than a forced split needs */
+};
+
+enum fp8g_kind {
+    FP8G_KIND_NT = 0,
+    FP8G_KIND_GROUPED_CONTIGUOUS = 1,
+    FP8G_KIND_GROUPED_MASKED = 2
+};
+
+/*
+ * Plain GEMM: D[M][N] = A[M][K] * B[N][K]^T with the scales above.
+ * Source: DeepGEMM fp8_gemm.cuh, fp8_gemm_kernel with GemmType::Normal.
+ * M == 0 or N == 0 is a no-op.  `workspace` (device memory, may be NULL) lets
+ * problems with fewer output tiles than SMs split K across SMs; its size
+ * comes from fp8_gemm_workspace_size.  It must be zero-filled before its
+ * first use; every successful call leaves it zero-filled again (after a
+ * device error, zero it again before reuse).  With no or too small a
+ * workspace the call runs unsplit and still returns FP8G_OK.
+ */
+int fp8_gemm_nt(const void *A, const float *SFA, const void *B, const float *SFB,
+                void *D, int M, int N, int K,
+                void *workspace, size_t workspace_bytes, fp8g_stream_t stream);
+
+/*
+ * Grouped GEMM, contiguous layout (MoE experts): rows of A are concatenated
+ * over groups; m_indices[r] (device int32 [M_total]) names the group of row
+ * r, and row r is multiplied by B[m_indices[r]].  Every 128-row block must
+ * hold one group: the kernel reads m_indices at the first row of each block.
+ * A block whose index is -1 is skipped and its D rows are left untouched;
+ * any other index outside [0, G) is skipped too and raises FP8G_ERR_BAD_GROUP
+ * in the device flag.
+ * Source: DeepGEMM fp8_gemm.cuh, GemmType::GroupedContiguous (B descriptor
+ * spans N * kNumGroups rows; the scheduler maps a block to its group).
+ */
+int fp8_gemm_grouped_contiguous(const void *A, const float *SFA, const void *B,
+                                const float *SFB, void *D, const int *m_indices,
+                                int M_total, int N, int K, int G,
+                                void *workspace, size_t workspace_bytes,
+                                fp8g_stream_t stream);
+
+/*
+ * Grouped GEMM, masked layout (MoE decode): group g computes rows
+ * 0 .. masked_m[g]-1 of its [M_max][K] slice of A against B[g]; D rows at or
+ * beyond masked_m[g] are left untouched.  masked_m is device int32 [G]; a
+ * count above M_max is clamped to M_max and a negative one treated as 0, both
+ * raising FP8G_ERR_BAD_GROUP in the device flag.
+ * Source: DeepGEMM fp8_gemm.cuh, GemmType::GroupedMasked (A, D and scales_a
+ * descriptors span kNumGroups slices of shape_m rows).
+ */
+int fp8_gemm_grouped_masked(const void *A, const float *SFA, const void *B,
+                            const float *SFB, void *D, const int *masked_m,
+                            int G, int M_max, int N, int K,
+                            void *workspace, size_t workspace_bytes,
+                            fp8g_stream_t stream);
+
+/*
+ * Bytes of workspace the given problem can use (0 if it never splits K).
+ * kind is an fp8g_kind; for NT pass G = 1; M is M, M_total or M_max.
+ * Pure host function: needs no GPU.  Assumes the current device's SM count
+ * if a device is present, else 152.
+ */
+size_t fp8_gemm_workspace_size(int kind, int M, int N, int K, int G);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's sticky
+ * device-side error (FP8G_OK if none; FP8G_ERR_TIMEOUT wins over
+ * FP8G_ERR_BAD_GROUP).  FP8G_ERR_CUDA if the synchronisation itself failed.
+ */
+int fp8_gemm_get_device_error(fp8g_stream_t stream);
+
+/* Static, human-readable text for a status code (never NULL). */
+const char *fp8_gemm_status_string(int status);
+
+/* Leading dimension of SFA for M rows: M rounded up to a multiple of 4. */
+int fp8_gemm_sfa_ld(int M);
+
+/*
+ * Tuning and test control (process-wide; 0 restores the automatic choice):
+ *   block_n     : 128 or 256 columns per output tile;
+ *   split_ctas  : > 0 forces the split-K schedule over that many CTAs (needs
+ *                 a workspace of fp8_gemm_workspace_size_for bytes), < 0
+ *                 forbids splitting.
+ * Returns FP8G_ERR_INVALID_ARG for values outside those sets.
+ */
+int fp8_gemm_set_override(int block_n, int split_ctas);
+
+/* Workspace bytes for an explicit split over `split_ctas` CTAs with tiles of
+ * `block_n` columns (the size fp8_gemm_workspace_size reports for the
+ * automatic choice). */
+size_t fp8_gemm_workspace_size_for(int M, int N, int K, int block_n, int split_ctas);
+
+/*
+ * Upper bound, in nanoseconds, on every pipeline wait inside the kernels
+ * (default 2e9).  A wait that runs out records FP8G_ERR_TIMEOUT, drains the
+ * block's copies in flight, frees its tensor memory and returns.  Must be >= 1e6.
+ */
+int fp8_gemm_set_wait_timeout_ns(uint64_t ns);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fp8_gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8GEMM_H */
