@@ -25,6 +25,7 @@ FP8G_ERR_CUDA = 4
 FP8G_ERR_TIMEOUT = 5
 FP8G_ERR_BAD_GROUP = 6
 FP8G_ERR_WORKSPACE = 7
+FP8G_ERR_SCRATCH_LIMIT = 8
 
 FP8G_KIND_NT = 0
 FP8G_KIND_GROUPED_CONTIGUOUS = 1
@@ -35,7 +36,7 @@ EXPORTS = (
     "fp8_gemm_nt", "fp8_gemm_grouped_contiguous", "fp8_gemm_grouped_masked",
     "fp8_gemm_workspace_size", "fp8_gemm_get_device_error", "fp8_gemm_status_string",
     "fp8_gemm_sfa_ld", "fp8_gemm_set_override", "fp8_gemm_workspace_size_for",
-    "fp8_gemm_set_wait_timeout_ns", "fp8_gemm_version",
+    "fp8_gemm_set_wait_timeout_ns", "fp8_gemm_nt_noalloc", "fp8_gemm_version",
 )
 
 _lock = threading.Lock()
@@ -78,6 +79,8 @@ def library(path: str = LIB_PATH):
         lib.fp8_gemm_set_override.restype = i
         lib.fp8_gemm_set_wait_timeout_ns.argtypes = [u64]
         lib.fp8_gemm_set_wait_timeout_ns.restype = i
+        lib.fp8_gemm_nt_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
+        lib.fp8_gemm_nt_noalloc.restype = i
         lib.fp8_gemm_version.argtypes = []
         lib.fp8_gemm_version.restype = i
         _lib = lib
@@ -163,6 +166,18 @@ def fp8_gemm_set_override(block_n=0, split_ctas=0) -> int:
 
 def fp8_gemm_set_wait_timeout_ns(ns) -> int:
     return library().fp8_gemm_set_wait_timeout_ns(int(ns))
+
+
+def fp8_gemm_nt_noalloc(A, SFA, B, SFB, D, M, N, K, stream=None) -> int:
+    """fp8_gemm_nt without a workspace, for callers that cannot call
+    cudaMalloc (code inside an allocator callback, plug-ins whose host
+    framework owns all device memory, loops that forbid allocation after
+    start-up).  The split-K scratch is a 24 MiB static device array inside the
+    library, so nothing is allocated per call.  Calls that overlap on the GPU
+    race on that one array; make the first call on a device before any
+    stream capture (it looks up the array's address)."""
+    return library().fp8_gemm_nt_noalloc(_ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D),
+                                         int(M), int(N), int(K), _stream(stream))
 
 
 def fp8_gemm_version() -> int:

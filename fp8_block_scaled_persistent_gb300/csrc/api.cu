@@ -388,6 +388,8 @@ const char *fp8_gemm_status_string(int status)
     case FP8G_ERR_TIMEOUT: return "a pipeline wait on the device ran out of time";
     case FP8G_ERR_BAD_GROUP: return "a group index or count was out of range";
     case FP8G_ERR_WORKSPACE: return "workspace too small for the forced split";
+    case FP8G_ERR_SCRATCH_LIMIT:
+        return "problem needs more split-K scratch than fp8_gemm_nt_noalloc's static buffer holds";
     default: return "unknown status";
     }
 }
@@ -416,3 +418,87 @@ int fp8_gemm_set_wait_timeout_ns(uint64_t ns)
 int fp8_gemm_version(void) { return kVersion; }
 
 }  // extern "C"
+
+// ============================================================================
+// fp8_gemm_nt_noalloc: the plain GEMM for callers that cannot call cudaMalloc
+// (code running inside an allocator callback, plug-ins whose host framework
+// owns all device memory, loops that forbid allocation after start-up) and so
+// cannot hand over a workspace.  The split-K schedule's scratch (ticket
+// counters and fp32 partials) lives in the static array below instead.
+
+namespace {
+
+// Largest scratch the split-K schedule may use through fp8_gemm_nt_noalloc.
+// It covers the schedule fp8_gemm_nt picks for any plain GEMM on a GPU with
+// up to 190 SMs (2 fp32 slots of 128 x 128 per CTA plus the tickets).
+constexpr size_t kNoAllocScratchBytes = size_t(24) << 20;
+
+// Every GPU that loads this library holds this array until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mutex;
+void *g_scratch_ptr[kMaxDevices];
+
+// Set-up, once per device, with that device current: the device address of
+// the static scratch.  (In host code the array's name is only a host-side
+// stand-in; the kernel must be given this address.)
+int noalloc_scratch(int dev, void **out)
+{
+    std::lock_guard<std::mutex> lk(g_scratch_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+            return FP8G_ERR_CUDA;
+        g_scratch_ptr[dev] = ptr;
+    }
+    *out = g_scratch_ptr[dev];
+    return FP8G_OK;
+}
+
+}  // namespace
+
+extern "C" int fp8_gemm_nt_noalloc(const void *A, const float *SFA, const void *B, const float *SFB,
+                                   void *D, int M, int N, int K, fp8g_stream_t stream)
+{
+    int st = check_common(A, SFA, B, SFB, D, M, N, K);
+    if (st != FP8G_OK)
+        return st;
+    if (M == 0 || N == 0)
+        return FP8G_OK;
+    DeviceInfo dev;
+    if ((st = current_device_info(dev)) != FP8G_OK)
+        return st;
+    int dev_id = 0;
+    if (cudaGetDevice(&dev_id) != cudaSuccess)
+        return FP8G_ERR_CUDA;
+    void *scratch = nullptr;
+    if ((st = noalloc_scratch(dev_id, &scratch)) != FP8G_OK)
+        return st;
+
+    // the same schedule fp8_gemm_nt picks when given all the workspace it asks for
+    NtChoice c;
+    if ((st = choose_nt(M, N, K, dev.sms, -1, c)) != FP8G_OK)
+        return st;
+    const size_t counters = ((size_t)c.tiles * 8 * sizeof(int) + 255) / 256 * 256;
+    if (c.split_ctas && split_workspace_bytes(M, N, K, 128, c.split_ctas) > kNoAllocScratchBytes)
+        return FP8G_ERR_SCRATCH_LIMIT;
+
+    LaunchArgs a;
+    fill_common(a.p, M, N, K, 1, SFA, SFB, D, nullptr, c.block_n, dev);
+    a.p.num_m_blocks = ceil_div(M, 128);
+    a.p.group_m = 8;
+    a.p.num_tiles = c.tiles;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    if (c.split_ctas) {
+        a.p.units = (long long)c.tiles * a.p.kb;
+        a.p.counters = static_cast<int *>(scratch);
+        a.p.partials = reinterpret_cast<float *>(static_cast<char *>(scratch) + counters);
+        // the array keeps the previous call's contents: the tickets start at zero
+        if (cudaMemsetAsync(scratch, 0, counters, a.stream) != cudaSuccess)
+            return FP8G_ERR_CUDA;
+    }
+    if (!make_maps(a, A, B, D, M, N, M, N, K, c.block_n))
+        return FP8G_ERR_CUDA;
+    a.grid = c.grid;
+    return to_status(fp8g::launch_nt(c.block_n, c.split_ctas != 0, a));
+}

@@ -64,7 +64,8 @@ enum fp8g_status {
     FP8G_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed           */
     FP8G_ERR_TIMEOUT = 5,      /* device: a bounded pipeline wait ran out     */
     FP8G_ERR_BAD_GROUP = 6,    /* device: group index / count out of range    */
-    FP8G_ERR_WORKSPACE = 7     /* workspace smaller than a forced split needs */
+    FP8G_ERR_WORKSPACE = 7,    /* workspace smaller than a forced split needs */
+    FP8G_ERR_SCRATCH_LIMIT = 8 /* fp8_gemm_nt_noalloc: static scratch too small */
 };
 
 enum fp8g_kind {
@@ -161,6 +162,33 @@ size_t fp8_gemm_workspace_size_for(int M, int N, int K, int block_n, int split_c
  * block's copies in flight, frees its tensor memory and returns.  Must be >= 1e6.
  */
 int fp8_gemm_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * fp8_gemm_nt_noalloc: fp8_gemm_nt for callers that cannot allocate device
+ * memory -- for example code that runs inside an allocator or memory-pool
+ * callback, plug-ins whose host framework owns every device allocation, or
+ * real-time loops that forbid allocation once they have started -- and so
+ * cannot provide the workspace the split-K schedule needs.  The paper has
+ * no counterpart to this entry point.
+ *
+ * Same operation, layouts, requirements and schedule as fp8_gemm_nt given
+ * all the workspace it asks for; the caller still passes A, SFA, B, SFB and
+ * D.  The split-K scratch (tickets and fp32 partials) is a static device
+ * array of 24 MiB (25,165,824 bytes) inside this library, enough for the
+ * schedule of any plain GEMM on a GPU with up to 190 SMs; every GPU that
+ * loads the library holds it until the process exits.  Nothing is allocated per call: no cudaMalloc, no cudaFree.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - A problem whose split-K schedule needs more scratch than the array
+ *     holds returns FP8G_ERR_SCRATCH_LIMIT and launches nothing.
+ *   - Every call shares the one array and clears its tickets (an async
+ *     memset on `stream`) before launching; calls that overlap on the GPU
+ *     (different streams, or several host threads) race on it and must be
+ *     serialised by the caller.
+ */
+int fp8_gemm_nt_noalloc(const void *A, const float *SFA, const void *B, const float *SFB,
+                        void *D, int M, int N, int K, fp8g_stream_t stream);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int fp8_gemm_version(void);
