@@ -21,7 +21,8 @@ SOURCES = ["api.cu", "gemm_nt.cu", "gemm_contiguous.cu", "gemm_masked.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-                     "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
+                     "--expt-relaxed-constexpr", "-Xptxas", "-v", "-I", os.path.join(ROOT, "include")]
+PTXAS_LOG = os.path.join(BUILD, "ptxas.log")
 
 
 def nvcc() -> str:
@@ -51,10 +52,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
         if verbose:
             sys.stderr.write(r.stdout + r.stderr)
-        return obj
+        return obj, r.stderr
 
     with ThreadPoolExecutor(len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
+        done = list(ex.map(compile_one, SOURCES))
+    objs = [o for o, _ in done]
+    # the register report of every kernel (checked by tests/test_build.py)
+    with open(PTXAS_LOG, "w") as f:
+        f.write("".join(log for _, log in done))
     tmp = LIB + f".tmp{os.getpid()}"
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
@@ -64,5 +69,4 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                extra_flags=["-Xptxas", "-v"] if "-v" in sys.argv else []))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

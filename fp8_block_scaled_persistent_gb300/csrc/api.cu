@@ -98,18 +98,21 @@ EncodeTiledFn encode_fn()
 
 // A 2-D row-major view: `inner` contiguous elements per row, `outer` rows,
 // `row_bytes` between rows; tiles of box_inner x box_outer elements.
+// outer == 0 makes a 1-D view of `inner` elements with boxes of box_inner.
+// Reads outside the view return zeros.
 bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc)
         return false;
+    const cuuint32_t rank = outer ? 2 : 1;
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {row_bytes};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t es[2] = {1, 1};
     std::memset(m, 0, sizeof(*m));
-    return enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    return enc(m, dt, rank, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -128,7 +131,7 @@ int check_common(const void *A, const float *SFA, const void *B, const float *SF
         return FP8G_ERR_UNSUPPORTED;
     if (rows > kMaxDim || N > kMaxDim || K > kMaxDim)
         return FP8G_ERR_UNSUPPORTED;
-    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16) || !aligned(SFA, 16) || !aligned(SFB, 4))
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16) || !aligned(SFA, 16) || !aligned(SFB, 16))
         return FP8G_ERR_MISALIGNED;
     return FP8G_OK;
 }
@@ -172,18 +175,23 @@ int choose_nt(int M, int N, int K, int sms, long long workspace_bytes, NtChoice 
     c.split_ctas = 0;
     const int kb = K / 128;
     const int o = g_override_split.load();
+    // the kernel's split arithmetic is 32-bit: units * CTAs must stay below 2^31
+    const long long units = (long long)c.tiles * kb;
+    auto split_fits = [&](long long P) { return units * P < (1ll << 31); };
     if (o > 0) {
         if (c.block_n != 128)
             return FP8G_ERR_INVALID_ARG;
-        const int P = (int)std::min<long long>(o, (long long)c.tiles * kb);
+        const int P = (int)std::min<long long>(o, units);
+        if (!split_fits(P))
+            return FP8G_ERR_UNSUPPORTED;
         if (workspace_bytes >= 0 && (long long)split_workspace_bytes(M, N, K, 128, P) > workspace_bytes)
             return FP8G_ERR_WORKSPACE;
         c.split_ctas = P;
     } else if (o == 0 && c.block_n == 128 && c.tiles < sms && kb >= 8) {
         // fewer output tiles than SMs: share the K blocks of all tiles evenly
         // over the SMs, at least 4 K blocks per CTA
-        const long long P = std::min<long long>(sms, (long long)c.tiles * kb / 4);
-        if (P > c.tiles &&
+        const long long P = std::min<long long>(sms, units / 4);
+        if (P > c.tiles && split_fits(P) &&
             (workspace_bytes < 0 ||
              (long long)split_workspace_bytes(M, N, K, 128, (int)P) <= workspace_bytes))
             c.split_ctas = (int)P;
@@ -214,15 +222,31 @@ void fill_common(Params &p, long long rows, int N, int K, int G, const float *SF
     p.timeout_ns = g_timeout_ns.load();
 }
 
-bool make_maps(LaunchArgs &a, const void *A, const void *B, void *D, long long a_rows, long long b_rows,
-               long long d_rows, int N, int K, int block_n)
+// The TMA swizzle that matches a staging panel's row width (2 bytes a column).
+CUtensorMapSwizzle panel_swizzle(int cols)
 {
+    return cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+}
+
+// Operand, output and scale views of one launch.  SFA is viewed as
+// [sfa_rows][sfa_ld] fp32 (sfa_rows = K/128, or G*K/128 when masked) and
+// loaded 128 rows' scales at a time; SFB as one flat fp32 vector of
+// G*ceil(N/128)*K/128 values, loaded in aligned groups of 4.
+bool make_maps(LaunchArgs &a, const void *A, const float *SFA, const void *B, const float *SFB, void *D,
+               long long a_rows, long long b_rows, long long d_rows, long long sfa_rows, int sfa_ld,
+               long long sfb_count, int N, int K, int block_n)
+{
+    const int pc = fp8g::panel_cols_for(block_n);
     return make_map(&a.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, a_rows, K, 128, 128,
                     CU_TENSOR_MAP_SWIZZLE_128B) &&
            make_map(&a.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, b_rows, K, 128, block_n,
                     CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_map(&a.tmap_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, N, d_rows, (uint64_t)N * 2, 32, 32,
-                    CU_TENSOR_MAP_SWIZZLE_64B);
+           make_map(&a.tmap_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, N, d_rows, (uint64_t)N * 2, pc, 32,
+                    panel_swizzle(pc)) &&
+           make_map(&a.tmap_sfa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SFA, sfa_ld, sfa_rows, (uint64_t)sfa_ld * 4,
+                    128, 1, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           make_map(&a.tmap_sfb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SFB, sfb_count, 0, 0, 4, 1,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace
@@ -255,12 +279,13 @@ int fp8_gemm_nt(const void *A, const float *SFA, const void *B, const float *SFB
     a.p.group_m = 8;
     a.p.num_tiles = c.tiles;
     if (c.split_ctas) {
-        a.p.units = (long long)c.tiles * a.p.kb;
+        a.p.units = c.tiles * a.p.kb;
         const size_t counters = ((size_t)c.tiles * 8 * sizeof(int) + 255) / 256 * 256;
         a.p.counters = static_cast<int *>(workspace);
         a.p.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + counters);
     }
-    if (!make_maps(a, A, B, D, M, N, M, N, K, c.block_n))
+    if (!make_maps(a, A, SFA, B, SFB, D, M, N, M, a.p.kb, a.p.sfa_ld, (long long)a.p.nb * a.p.kb, N, K,
+                   c.block_n))
         return FP8G_ERR_CUDA;
     a.grid = c.grid;
     a.stream = reinterpret_cast<cudaStream_t>(stream);
@@ -294,7 +319,8 @@ int fp8_gemm_grouped_contiguous(const void *A, const float *SFA, const void *B, 
     a.p.num_m_blocks = mb;
     a.p.group_m = 8;
     a.p.num_tiles = mb * a.p.num_n_blocks;
-    if (!make_maps(a, A, B, D, M_total, (long long)G * N, M_total, N, K, block_n))
+    if (!make_maps(a, A, SFA, B, SFB, D, M_total, (long long)G * N, M_total, a.p.kb, a.p.sfa_ld,
+                   (long long)G * a.p.nb * a.p.kb, N, K, block_n))
         return FP8G_ERR_CUDA;
     a.grid = std::min(dev.sms, a.p.num_tiles);
     a.stream = reinterpret_cast<cudaStream_t>(stream);
@@ -329,7 +355,8 @@ int fp8_gemm_grouped_masked(const void *A, const float *SFA, const void *B, cons
     a.p.num_m_blocks = mb;
     a.p.group_m = mb;   // all m-blocks of a (group, n-block) run together: B is read once
     const long long tiles_max = (long long)G * mb * a.p.num_n_blocks;
-    if (!make_maps(a, A, B, D, (long long)G * M_max, (long long)G * N, (long long)G * M_max, N, K, block_n))
+    if (!make_maps(a, A, SFA, B, SFB, D, (long long)G * M_max, (long long)G * N, (long long)G * M_max,
+                   (long long)G * a.p.kb, a.p.sfa_ld, (long long)G * a.p.nb * a.p.kb, N, K, block_n))
         return FP8G_ERR_CUDA;
     a.grid = (int)std::min<long long>(dev.sms, tiles_max);
     a.stream = reinterpret_cast<cudaStream_t>(stream);
@@ -383,7 +410,7 @@ const char *fp8_gemm_status_string(int status)
     case FP8G_OK: return "ok";
     case FP8G_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or G <= 0)";
     case FP8G_ERR_UNSUPPORTED: return "unsupported shape (needs K % 128 == 0, N % 16 == 0, M_total % 128 == 0)";
-    case FP8G_ERR_MISALIGNED: return "misaligned pointer (A, B, D, SFA need 16 bytes, SFB 4, workspace 256)";
+    case FP8G_ERR_MISALIGNED: return "misaligned pointer (A, B, D, SFA, SFB need 16 bytes, workspace 256)";
     case FP8G_ERR_CUDA: return "a CUDA call failed";
     case FP8G_ERR_TIMEOUT: return "a pipeline wait on the device ran out of time";
     case FP8G_ERR_BAD_GROUP: return "a group index or count was out of range";
@@ -490,14 +517,15 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const float *SFA, const void *
     a.p.num_tiles = c.tiles;
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     if (c.split_ctas) {
-        a.p.units = (long long)c.tiles * a.p.kb;
+        a.p.units = c.tiles * a.p.kb;
         a.p.counters = static_cast<int *>(scratch);
         a.p.partials = reinterpret_cast<float *>(static_cast<char *>(scratch) + counters);
         // the array keeps the previous call's contents: the tickets start at zero
         if (cudaMemsetAsync(scratch, 0, counters, a.stream) != cudaSuccess)
             return FP8G_ERR_CUDA;
     }
-    if (!make_maps(a, A, B, D, M, N, M, N, K, c.block_n))
+    if (!make_maps(a, A, SFA, B, SFB, D, M, N, M, a.p.kb, a.p.sfa_ld, (long long)a.p.nb * a.p.kb, N, K,
+                   c.block_n))
         return FP8G_ERR_CUDA;
     a.grid = c.grid;
     return to_status(fp8g::launch_nt(c.block_n, c.split_ctas != 0, a));

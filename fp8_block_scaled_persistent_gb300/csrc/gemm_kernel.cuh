@@ -7,21 +7,28 @@
 // the accumulator is rounded to bf16 at the end.
 //
 // How, on Blackwell (design ours; the DeepGEMM page's Hopper kernel and the
-// "TCGen05 Copy Instruction" tutorial's warp-specialised matmul are prior art):
+// "TCGen05 Copy Instruction" tutorial's warp-specialised matmul are prior art).
+// Three warpgroups of four warps:
 //   warp 0      TMA producer: 128x128 A and BNx128 B e4m3 tiles, 128-byte
-//               swizzled, into an S-stage shared-memory ring (full/empty
-//               mbarriers, transaction-count completion).
+//               swizzled, into an S-stage shared-memory ring, and the K block's
+//               scales (128 A scales, the B scales of the tile's 128-column
+//               blocks) into a deeper scale ring.  mbarrier transaction counts
+//               signal completion.
 //   warp 1      MMA issuer: one thread issues 4 x tcgen05.mma kind::f8f6f4
 //               (128 x BN x 32) per K block into a FRESH tensor-memory buffer
-//               (the first MMA overwrites), then commits the stage back to the
-//               producer and the buffer to the epilogue.  512 TMEM columns
-//               hold 512/BN such buffers, so the MMA of block k+1 runs while
-//               block k is being promoted.
-//   warps 2..9  epilogue: tcgen05.ld of the K block's partial, promotion
+//               (the first MMA overwrites) and commits once per K block.  That
+//               one commit both frees the operand stage and tells the
+//               epilogue the buffer is complete: each commit drains the tensor
+//               pipe, so there is only one.  512 TMEM columns hold 512/BN
+//               buffers, so the MMA of block k+1 runs while k is promoted.
+//   warps 2-3   idle (they only give their registers away).
+//   warps 4-11  epilogue: tcgen05.ld of the K block's partial, promotion
 //               acc += (sa*sb) * P in fp32 registers (one row per thread,
 //               BN/2 columns per warp), and at the end of a tile bf16
-//               conversion into a 64-byte-swizzled staging panel and a TMA
-//               store (or predicated stores where masked rows straddle).
+//               conversion into swizzled staging panels and TMA stores (or
+//               predicated stores where masked rows straddle).
+// Registers: the control warpgroup drops to kRegsCtl with setmaxnreg and the
+// epilogue warpgroups rise to kRegsEpi (the accumulator is BN/2 registers).
 //   scheduler   persistent: CTA c takes tiles c, c+P, ... in a banded
 //               rasterisation (m fastest inside a band of m-blocks); grouped
 //               layouts map tiles to groups.  A split-K ("stream-K") variant
@@ -41,32 +48,72 @@
 #include "gemm_params.h"
 #include "ptx.cuh"
 
+#ifndef FP8G_STAGES_256
+#define FP8G_STAGES_256 3
+#endif
+#ifndef FP8G_FULL_TILE_STAGING
+#define FP8G_FULL_TILE_STAGING 1
+#endif
+#ifndef FP8G_PANEL_COLS_FULL
+#define FP8G_PANEL_COLS_FULL 64
+#endif
+
 namespace fp8g {
 
 constexpr int kBM = 128;
 constexpr int kBK = 128;
-constexpr int kNumThreads = 320;      // 10 warps
-constexpr int kEpiWarp0 = 2;
+constexpr int kNumThreads = 384;      // 3 warpgroups of 4 warps
+constexpr int kEpiWarp0 = 4;          // warpgroups 1 and 2 are the epilogue
 constexpr int kNumEpiWarps = 8;
 constexpr int kTmemCols = 512;
-constexpr int kPanelCols = 32;        // bf16 columns per staging panel (64 B rows)
-constexpr int kPanelBytes = 32 * kPanelCols * 2;
+// Registers per thread after reallocation: warpgroup 0 (producer, MMA, two
+// idle warps) gives registers to the epilogue warpgroups.  The launch
+// allocation is 384 x 168 = 64512; 128 x 40 + 256 x 232 = 64512.
+constexpr int kRegsCtl = 40;
+constexpr int kRegsEpi = 232;
+constexpr int kLaunchRegs = 168;
+static_assert(128 * kRegsCtl + 256 * kRegsEpi <= kNumThreads * kLaunchRegs,
+              "register reallocation exceeds the launch allocation");
 
 enum Kind : int { kKindNT = 0, kKindContiguous = 1, kKindMasked = 2 };
 
 template <int BN>
 struct Cfg {
     static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
-    static constexpr int kStages = (BN == 256) ? 4 : 6;
-    static constexpr int kAccBufs = kTmemCols / BN;
-    static constexpr int kABytes = kBM * kBK;           // e4m3
+    // With whole-tile staging the epilogue drops a whole bf16 tile into
+    // shared memory and moves on; TMA stores drain it during the next tile.
+    static constexpr bool kFullTileStaging = BN == 256 && FP8G_FULL_TILE_STAGING != 0;
+    static constexpr int kStages = (BN == 256) ? FP8G_STAGES_256 : 6;   // A/B operand ring
+    static constexpr int kAccBufs = kTmemCols / BN;                     // TMEM partial buffers
+    static constexpr int kScaleSlots = kStages + kAccBufs;              // scale ring: never the limiter
+    static constexpr int kABytes = kBM * kBK;                           // e4m3
     static constexpr int kBBytes = BN * kBK;
     static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kSfbRows = BN / 128;                           // 128-column blocks per tile
+    // scale slot: 128 A scales (one per tile row), then per column block a
+    // 16-byte group of 4 consecutive B scales that holds this K block's one.
+    // Every TMA destination in shared memory starts on a 128-byte boundary.
+    static constexpr int kSlotSfaBytes = kBM * 4;
+    static constexpr int kSlotSfbStride = 128;
+    static constexpr int kSlotBytes = kSlotSfaBytes + kSlotSfbStride * kSfbRows;
+    static constexpr int kSlotTxBytes = kSlotSfaBytes + 16 * kSfbRows;
     static constexpr int kColsPerThread = BN / 2;
-    static constexpr int kStagingBytes = kNumEpiWarps * 2 * kPanelBytes;
-    static constexpr int kBarrierBytes = (2 * kStages + 2 * kAccBufs + 1) * 8;
-    static constexpr int kSmemBytes =
-        kStages * kStageBytes + kStagingBytes + kBarrierBytes + 64 + 1024 /* alignment slack */;
+    // output panels: 32 rows x kPanelCols bf16, TMA-stored with the swizzle
+    // of their row width
+    static constexpr int kPanelCols = kFullTileStaging ? FP8G_PANEL_COLS_FULL : 16;
+    static constexpr int kPanelBytes = 32 * kPanelCols * 2;
+    static constexpr int kPanelsPerWarp = kFullTileStaging ? (BN / 2) / kPanelCols : 2;
+    static constexpr int kStagingBytes = kNumEpiWarps * kPanelsPerWarp * kPanelBytes;
+    static constexpr int kBarriers = 2 * kStages + kAccBufs + 2 * kScaleSlots + 1;
+    static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + kScaleSlots * kSlotBytes +
+                                      kBarriers * 8 + 16 + 1024 /* alignment slack */;
+    static_assert(kSlotTxBytes <= kSlotBytes, "scale slot");
+    static_assert(kSlotBytes % 128 == 0 && kSlotSfaBytes % 128 == 0 && kStagingBytes % 1024 == 0 &&
+                      kABytes % 1024 == 0 && kBBytes % 1024 == 0 && kPanelBytes % 1024 == 0,
+                  "TMA destinations and sources must stay 128-byte (swizzled: 1024-byte) aligned");
+    static_assert(kPanelCols == 16 || kPanelCols == 32 || kPanelCols == 64, "panel width");
+    static_assert(kStages >= kAccBufs, "the epilogue's wait on a stage's MMA completion must not alias");
+    static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
 struct Work {
@@ -104,7 +151,7 @@ template <int BN, int KIND, bool SPLIT>
 struct Scheduler {
     const Params &p;
     int next_tile;
-    long long u, u_end;
+    int u, u_end;
     int walk_g = 0, walk_base = 0, walk_tiles = -1, walk_count = 0;
     bool report;
 
@@ -117,9 +164,10 @@ struct Scheduler {
         }
     }
 
-    __device__ __forceinline__ long long unit_begin(int c) const
+    // the host keeps units * CTAs below 2^31
+    __device__ __forceinline__ int unit_begin(int c) const
     {
-        return (long long)c * p.units / (long long)gridDim.x;
+        return (int)((unsigned)c * (unsigned)p.units / gridDim.x);
     }
 
     __device__ __forceinline__ int clamp_count(int g) const
@@ -133,10 +181,9 @@ struct Scheduler {
         if constexpr (SPLIT) {
             if (u >= u_end)
                 return false;
-            const int t = (int)(u / p.kb);
-            const int k0 = (int)(u - (long long)t * p.kb);
-            const long long left = u_end - u;
-            const int k1 = (int)min((long long)p.kb, (long long)k0 + left);
+            const int t = u / p.kb;
+            const int k0 = u - t * p.kb;
+            const int k1 = min(p.kb, k0 + (u_end - u));
             u += k1 - k0;
             raster(t, p.num_m_blocks, p.num_n_blocks, p.group_m, w.m_blk, w.n_blk);
             w.g = 0;
@@ -210,35 +257,41 @@ struct Scheduler {
 
 // Owner CTA of split unit v when U units are shared by P CTAs in equal
 // contiguous ranges [floor(c*U/P), floor((c+1)*U/P)).
-__device__ __forceinline__ int unit_owner(long long v, long long U, int P)
+__device__ __forceinline__ int unit_owner(int v, int U, int P)
 {
-    return (int)(((v + 1) * (long long)P - 1) / U);
+    return (int)(((unsigned)(v + 1) * (unsigned)P - 1u) / (unsigned)U);
 }
 
 // ----------------------------------------------------------------------------
 // Epilogue helpers
 
-// Writes 32 columns (one staging panel) of this warp's 32 rows to D.
-// acc32 holds this thread's row, columns x .. x+31 of the output.
-__device__ __forceinline__ void store_panel(const float *acc32, uint8_t *panel, const CUtensorMap *tmap_d,
-                                            const Params &p, int x, int y_row0, int rows_ok, int lane,
-                                            bool tma_ok)
+// Writes PC columns (one staging panel) of this warp's 32 rows to D.
+// accp holds this thread's row, columns x .. x+PC-1 of the output.
+template <int PC, bool kWaitBuffer>
+__device__ __forceinline__ void store_panel(const float *accp, uint8_t *panel, const CUtensorMap *tmap_d,
+                                            const Params &p, int x, int y_row0, int rows_ok, int lane)
 {
-    // 16-byte chunk c of row `lane` sits at chunk position c ^ ((lane >> 1) & 3)
-    // of its 64-byte row (the 64-byte swizzle the D tensor map uses).
-    uint32_t w[16];
+    constexpr int NW = PC / 2;          // bf16x2 words per row
+    constexpr int NC = PC / 8;          // 16-byte chunks per row
+    uint32_t w[NW];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-        w[i] = pack_bf16x2(acc32[2 * i], acc32[2 * i + 1]);
-    if (tma_ok && rows_ok == 32) {
-        if (lane == 0)
-            bulk_wait_group_read<1>();
-        __syncwarp();
-        const uint32_t base = smem_u32(panel) + lane * 64;
+    for (int i = 0; i < NW; ++i)
+        w[i] = pack_bf16x2(accp[2 * i], accp[2 * i + 1]);
+    if (rows_ok == 32) {
+        // all 32 rows belong in D: stage the panel and let TMA store it.
+        // TMA's swizzle XORs the 16-byte chunk index with address bits 7..9:
+        // chunk c of row r sits at c ^ ((r * row_bytes) >> 7 & (NC - 1)).
+        if (kWaitBuffer) {
+            // two alternating panel buffers: the one before last must be read
+            if (lane == 0)
+                bulk_wait_group_read<1>();
+            __syncwarp();
+        }
+        const uint32_t base = smem_u32(panel) + lane * (PC * 2);
+        const int sw = ((lane * PC * 2) >> 7) & (NC - 1);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            st_shared_v4(base + ((c ^ ((lane >> 1) & 3)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2],
-                         w[4 * c + 3]);
+        for (int c = 0; c < NC; ++c)
+            st_shared_v4(base + ((c ^ sw) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) {
@@ -249,9 +302,57 @@ __device__ __forceinline__ void store_panel(const float *acc32, uint8_t *panel, 
         // predicated row stores: only rows that belong in D are written
         uint4 *dst = reinterpret_cast<uint4 *>(p.d + (size_t)(y_row0 + lane) * p.N + x);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < NC; ++c)
             if (x + 8 * c < p.N)
                 dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Epilogue: per-K-block promotion
+
+template <int N>
+__device__ __forceinline__ void fma_cols(float *acc, const uint32_t (&v)[N], float s)
+{
+    const float2 s2 = make_float2(s, s);
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+        float2 a2 = make_float2(acc[i], acc[i + 1]);
+        a2 = __ffma2_rn(s2, make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), a2);
+        acc[i] = a2.x;
+        acc[i + 1] = a2.y;
+    }
+}
+
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld_32x32b_x16(taddr, r); }
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld_32x32b_x32(taddr, r); }
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[64]) { tmem_ld_32x32b_x64(taddr, r); }
+
+__device__ __forceinline__ void release_tmem(uint64_t *bar, int lane)
+{
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(bar);
+}
+
+// acc[0 .. COLS) += s * (this thread's row of the K block's partial in TMEM,
+// columns taddr.col .. +COLS), LD columns per tcgen05.ld.  The buffer is
+// handed back to the MMA issuer as soon as its last load landed.
+template <int COLS, int LD>
+__device__ __forceinline__ void promote_block(float (&acc)[COLS], uint32_t taddr, float s, uint64_t *tempty_bar,
+                                              int lane)
+{
+    constexpr int NCH = COLS / LD;
+    static_assert(COLS % LD == 0, "column split");
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+        uint32_t v[LD];
+        tmem_ld(taddr + c * LD, v);
+        tmem_wait_ld(v);
+        if (c + 1 == NCH)
+            release_tmem(tempty_bar, lane);
+        fma_cols<LD>(acc + c * LD, v, s);
     }
 }
 
@@ -261,25 +362,30 @@ __device__ __forceinline__ void store_panel(const float *acc32, uint8_t *panel, 
 template <int BN, int KIND, bool SPLIT>
 __global__ void __launch_bounds__(kNumThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                    const __grid_constant__ CUtensorMap tmap_d, const Params p)
+                    const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_sfa,
+                    const __grid_constant__ CUtensorMap tmap_sfb, const __grid_constant__ Params p)
 {
 #if defined(__CUDA_ARCH__)
     using C = Cfg<BN>;
     constexpr int S = C::kStages;
     constexpr int NACC = C::kAccBufs;
+    constexpr int SR = C::kScaleSlots;
     constexpr int COLS = C::kColsPerThread;
 
+    // shared memory: [A stages][B stages][D staging][scale slots][barriers][tmem addr, abort]
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sm_a = smem;
     uint8_t *sm_b = sm_a + S * C::kABytes;
     uint8_t *sm_stage_d = sm_b + S * C::kBBytes;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm_stage_d + C::kStagingBytes);
-    uint64_t *full = bar;
-    uint64_t *empty = full + S;
-    uint64_t *tfull = empty + S;
-    uint64_t *tempty = tfull + NACC;
-    uint64_t *drain = tempty + NACC;
+    uint8_t *sm_scales = sm_stage_d + C::kStagingBytes;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm_scales + SR * C::kSlotBytes);
+    uint64_t *full = bar;              // S:  A/B tiles landed (TMA transactions)
+    uint64_t *empty = full + S;        // S:  MMAs of the stage finished (one commit per K block)
+    uint64_t *tempty = empty + S;      // NACC: epilogue finished reading a TMEM buffer
+    uint64_t *sfull = tempty + NACC;   // SR: scale slot landed (TMA transactions)
+    uint64_t *sempty = sfull + SR;     // SR: epilogue finished reading a scale slot
+    uint64_t *drain = sempty + SR;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -291,9 +397,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
-        for (int i = 0; i < NACC; ++i) {
-            mbar_init(&tfull[i], 1);
+        for (int i = 0; i < NACC; ++i)
             mbar_init(&tempty[i], kNumEpiWarps);
+        for (int i = 0; i < SR; ++i) {
+            mbar_init(&sfull[i], 1);
+            mbar_init(&sempty[i], kNumEpiWarps);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -304,6 +412,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         prefetch_tensormap(&tmap_a);
         prefetch_tensormap(&tmap_b);
         prefetch_tensormap(&tmap_d);
+        prefetch_tensormap(&tmap_sfa);
+        prefetch_tensormap(&tmap_sfb);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
@@ -316,37 +426,54 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     const WaitCtl ctl{abort_flag, p.error_word, p.timeout_ns};
 
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
+    // Each role sits inside the branch that sets its register budget, so the
+    // epilogue is only reachable with the larger one.
+    if (warp < kEpiWarp0) {
+        regs_dealloc<kRegsCtl>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------ TMA producer
             Scheduler<BN, KIND, SPLIT> sched(p, false);
             Work w;
-            Ring ring;
-            uint32_t issued = 0, issued_parity = 0;
+            Ring ring, sring;
+            uint32_t issued = 0, issued_parity = 0, sissued = 0, sissued_parity = 0;
             bool ok = true;
             while (ok && sched.next(w)) {
                 const int b_row0 = w.g * p.N + w.n_blk * BN;
+                const int sfa_y0 = (KIND == kKindMasked) ? w.g * p.kb : 0;
+                const int sfb_x0 = (w.g * p.nb + (w.n_blk * BN) / 128) * p.kb;
                 for (int k = w.kb0; k < w.kb1; ++k) {
-                    if (!mbar_wait(&empty[ring.i], ring.ph ^ 1u, ctl)) {
+                    if (!mbar_wait(&empty[ring.i], ring.ph ^ 1u, ctl) ||
+                        !mbar_wait(&sempty[sring.i], sring.ph ^ 1u, ctl)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(&full[ring.i], C::kStageBytes);
                     tma_load_2d(sm_a + ring.i * C::kABytes, &tmap_a, &full[ring.i], k * kBK, w.a_row0);
                     tma_load_2d(sm_b + ring.i * C::kBBytes, &tmap_b, &full[ring.i], k * kBK, b_row0);
+                    uint8_t *slot = sm_scales + sring.i * C::kSlotBytes;
+                    mbar_arrive_expect_tx(&sfull[sring.i], C::kSlotTxBytes);
+                    tma_load_2d(slot, &tmap_sfa, &sfull[sring.i], w.m_blk * kBM, sfa_y0 + k);
+#pragma unroll
+                    for (int j = 0; j < C::kSfbRows; ++j)
+                        tma_load_1d(slot + C::kSlotSfaBytes + C::kSlotSfbStride * j, &tmap_sfb, &sfull[sring.i],
+                                    (sfb_x0 + j * p.kb + k) & ~3);
                     issued |= 1u << ring.i;
                     issued_parity = (issued_parity & ~(1u << ring.i)) | (ring.ph << ring.i);
+                    sissued |= 1u << sring.i;
+                    sissued_parity = (sissued_parity & ~(1u << sring.i)) | (sring.ph << sring.i);
                     ring.template next<S>();
+                    sring.template next<SR>();
                 }
             }
             // every fill this thread started has landed before the CTA exits
-            for (int s = 0; s < S; ++s)
-                if (issued & (1u << s))
-                    mbar_wait_drain(&full[s], (issued_parity >> s) & 1u, p.timeout_ns);
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+            for (int i = 0; i < S; ++i)
+                if (issued & (1u << i))
+                    mbar_wait_drain(&full[i], (issued_parity >> i) & 1u, p.timeout_ns);
+            for (int i = 0; i < SR; ++i)
+                if (sissued & (1u << i))
+                    mbar_wait_drain(&sfull[i], (sissued_parity >> i) & 1u, p.timeout_ns);
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------ MMA issuer
             Scheduler<BN, KIND, SPLIT> sched(p, false);
             Work w;
             Ring ring, acc;
@@ -365,8 +492,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kBK / 32; ++kk)  // +32 bytes along K = +2 in the address field
                         mma_f8f6f4(d_tmem, a0 + 2 * kk, b0 + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+                    // One commit per K block (each commit drains the tensor
+                    // pipe): it frees the operand stage for the producer and
+                    // tells the epilogue that TMEM buffer acc.i is complete.
                     mma_commit(&empty[ring.i]);
-                    mma_commit(&tfull[acc.i]);
                     ring.template next<S>();
                     acc.template next<NACC>();
                 }
@@ -376,13 +505,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_wait_drain(drain, 0, p.timeout_ns);
         }
     } else {
+        regs_alloc<kRegsEpi>();
         // ------------------------------------------------ epilogue warps
         const int ew = warp - kEpiWarp0;     // 0..7
         const int q = warp & 3;              // TMEM lane quarter this warp may access
         const int h = ew >> 2;               // column half of the tile
         const int row_in_tile = 32 * q + lane;
-        uint8_t *panels = sm_stage_d + ew * 2 * kPanelBytes;
+        const int sfb_row = (BN == 256) ? h : 0;
+        uint8_t *panels = sm_stage_d + ew * C::kPanelsPerWarp * C::kPanelBytes;
         uint32_t panel_ctr = 0;
+        (void)panel_ctr;
 
         if (KIND == kKindMasked && blockIdx.x == 0 && ew == 0) {
             for (int g = lane; g < p.G; g += 32) {
@@ -394,7 +526,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
         Scheduler<BN, KIND, SPLIT> sched(p, ew == 0 && lane == 0);
         Work w;
-        Ring acc_ring;
+        Ring ring, acc_ring, sring;
         bool ok = true;
         while (ok && sched.next(w)) {
             float acc[COLS];
@@ -402,75 +534,39 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             for (int i = 0; i < COLS; ++i)
                 acc[i] = 0.f;
 
-            // scale sources for this thread's row and this warp's 128-column block
-            const int m_local = w.m_blk * kBM + row_in_tile;              // row inside the group
-            const bool row_ok = m_local < p.rows;
-            const float *sfa_row =
-                p.sfa + (KIND == kKindMasked ? (size_t)w.g * p.kb * p.sfa_ld : 0) + m_local;
-            const int nbc = (w.n_blk * BN + h * COLS) / 128;
-            const bool col_ok = nbc < p.nb;
-            const float *sfb_row = p.sfb + ((size_t)w.g * p.nb + nbc) * p.kb;
-
-            float sa_cur = row_ok ? ld_nc_f32(sfa_row + (size_t)w.kb0 * p.sfa_ld) : 0.f;
-            int chunk = w.kb0 & ~31;
-            float sb_cur = (col_ok && chunk + lane < p.kb) ? ld_nc_f32(sfb_row + chunk + lane) : 0.f;
-            float sb_nxt = 0.f;
-
             for (int k = w.kb0; k < w.kb1; ++k) {
-                // prefetch the next K block's A scale and, at a 32-block
-                // boundary, the next chunk of B scales
-                const float sa_nxt =
-                    (row_ok && k + 1 < w.kb1) ? ld_nc_f32(sfa_row + (size_t)(k + 1) * p.sfa_ld) : 0.f;
-                if ((k & 31) == 0 && k != w.kb0)
-                    sb_cur = sb_nxt;
-                if ((k & 31) == 0 || k == w.kb0) {
-                    const int nc = (k & ~31) + 32;
-                    sb_nxt = (col_ok && nc + lane < p.kb && nc < w.kb1) ? ld_nc_f32(sfb_row + nc + lane) : 0.f;
-                }
-                const float sb = __shfl_sync(0xffffffffu, sb_cur, k & 31);
-                const float s = sa_cur * sb;
-                sa_cur = sa_nxt;
-
+                // the K block's scales (landed long ago: the producer runs
+                // up to S + NACC blocks ahead), then its MMA completion.  The
+                // stage barrier cannot have moved on: MMA k+S needs the TMEM
+                // buffer this warp frees after block k+S-NACC >= k.
                 int got = 1;
                 if (lane == 0)
-                    got = mbar_wait(&tfull[acc_ring.i], acc_ring.ph, ctl) ? 1 : 0;
+                    got = (mbar_wait(&sfull[sring.i], sring.ph, ctl) && mbar_wait(&empty[ring.i], ring.ph, ctl)) ? 1
+                                                                                                               : 0;
                 got = __shfl_sync(0xffffffffu, got, 0);
                 if (!got) {
                     ok = false;
                     break;
                 }
+                __syncwarp();           // orders lane 0's barrier waits before every lane's reads
                 tc_fence_after_sync();
+                const uint8_t *slot = sm_scales + sring.i * C::kSlotBytes;
+                const float sa = reinterpret_cast<const float *>(slot)[row_in_tile];
+                // the slot holds the aligned group of 4 around this K block's
+                // B scale: its flat index in SFB picks the element
+                const int sfb_idx = (w.g * p.nb + (w.n_blk * BN) / 128 + sfb_row) * p.kb + k;
+                const float sb =
+                    reinterpret_cast<const float *>(slot + C::kSlotSfaBytes + C::kSlotSfbStride * sfb_row)[sfb_idx & 3];
+                const float s = sa * sb;
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sempty[sring.i]);
+                sring.template next<SR>();
 
                 const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + acc_ring.i * BN + h * COLS;
-                uint32_t v0[16], v1[16];
-                tmem_ld_32x32b_x16(taddr, v0);
-                tmem_wait_ld(v0);
-#pragma unroll
-                for (int c = 0; c < COLS / 16; ++c) {
-                    uint32_t(&cur)[16] = (c & 1) ? v1 : v0;
-                    uint32_t(&nxt)[16] = (c & 1) ? v0 : v1;
-                    if (c + 1 < COLS / 16)
-                        tmem_ld_32x32b_x16(taddr + 16 * (c + 1), nxt);
-#pragma unroll
-                    for (int i = 0; i < 16; i += 2) {
-                        float2 a2 = make_float2(acc[16 * c + i], acc[16 * c + i + 1]);
-                        const float2 p2 = make_float2(__uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
-                        a2 = __ffma2_rn(make_float2(s, s), p2, a2);
-                        acc[16 * c + i] = a2.x;
-                        acc[16 * c + i + 1] = a2.y;
-                    }
-                    if (c + 1 < COLS / 16) {
-                        tmem_wait_ld(nxt);
-                        if (c + 2 == COLS / 16) {
-                            // every column of this buffer is in registers now
-                            tc_fence_before_sync();
-                            __syncwarp();
-                            if (lane == 0)
-                                mbar_arrive(&tempty[acc_ring.i]);
-                        }
-                    }
-                }
+                promote_block<COLS, 64>(acc, taddr, s, &tempty[acc_ring.i], lane);
                 acc_ring.template next<NACC>();
+                ring.template next<S>();
             }
             if (!ok)
                 break;
@@ -482,11 +578,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     // sums all partials in CTA order and stores the tile.
                     const int t = w.tile;
                     const int P = gridDim.x;
-                    const int c_lo = unit_owner((long long)t * p.kb, p.units, P);
-                    const int c_hi = unit_owner((long long)(t + 1) * p.kb - 1, p.units, P);
+                    const int c_lo = unit_owner(t * p.kb, p.units, P);
+                    const int c_hi = unit_owner((t + 1) * p.kb - 1, p.units, P);
                     auto slot_of = [&](int c) {
-                        const long long first_tile = ((long long)c * p.units / P) / p.kb;
-                        return 2 * c + ((long long)t == first_tile ? 0 : 1);
+                        const int first_tile = (int)((unsigned)c * (unsigned)p.units / (unsigned)P) / p.kb;
+                        return 2 * c + (t == first_tile ? 0 : 1);
                     };
                     constexpr int F4 = COLS / 4;
                     auto region = [&](int c) {
@@ -535,16 +631,29 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // ---- bf16 store of this warp's 32 rows x COLS columns
             const int rows_ok = min(max(w.valid_rows - 32 * q, 0), 32);
             const int y_row0 = w.a_row0 + 32 * q;
+            if constexpr (C::kFullTileStaging) {
+                // the previous tile's stores have had a whole tile to read
+                // this warp's staging area; make sure they are done
+                if (lane == 0)
+                    bulk_wait_group_read<0>();
+                __syncwarp();
+            }
+            constexpr int PC = C::kPanelCols;
 #pragma unroll
-            for (int pi = 0; pi < COLS / kPanelCols; ++pi) {
-                const int x = w.n_blk * BN + h * COLS + pi * kPanelCols;
+            for (int pi = 0; pi < COLS / PC; ++pi) {
+                const int x = w.n_blk * BN + h * COLS + pi * PC;
                 if (x >= p.N || rows_ok == 0)
                     continue;
-                uint8_t *panel = panels + (panel_ctr & 1u) * kPanelBytes;
-                // TMA stores may be used unless masked rows straddle this slab
-                store_panel(acc + pi * kPanelCols, panel, &tmap_d, p, x, y_row0, rows_ok, lane, true);
-                if (rows_ok == 32)
-                    ++panel_ctr;
+                // TMA store unless the slab's rows straddle the end of D's rows
+                if constexpr (C::kFullTileStaging) {
+                    store_panel<PC, false>(acc + pi * PC, panels + pi * C::kPanelBytes, &tmap_d, p, x, y_row0,
+                                           rows_ok, lane);
+                } else {
+                    uint8_t *buf = panels + (panel_ctr & 1u) * C::kPanelBytes;
+                    store_panel<PC, true>(acc + pi * PC, buf, &tmap_d, p, x, y_row0, rows_ok, lane);
+                    if (rows_ok == 32)
+                        ++panel_ctr;
+                }
             }
         }
         if (lane == 0)

@@ -9,6 +9,11 @@ int smem_bytes_for(int block_n)
     return block_n == 256 ? Cfg<256>::kSmemBytes : Cfg<128>::kSmemBytes;
 }
 
+int panel_cols_for(int block_n)
+{
+    return block_n == 256 ? Cfg<256>::kPanelCols : Cfg<128>::kPanelCols;
+}
+
 cudaError_t launch_nt(int block_n, bool split, const LaunchArgs &a)
 {
     if (split)

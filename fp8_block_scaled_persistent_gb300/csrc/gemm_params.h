@@ -21,7 +21,7 @@ struct Params {
     int num_n_blocks;  // ceil(N/BN)
     int group_m;       // rasterisation band height, in m-blocks
     int num_tiles;     // NT and contiguous
-    long long units;   // split: num_tiles * kb
+    int units;         // split: num_tiles * kb (the host keeps units * CTAs < 2^31)
     float *partials;   // split: 2 * gridDim.x slots of 128 x BN fp32
     int *counters;     // split: num_tiles * 8 tickets
     int *error_word;

@@ -10,7 +10,7 @@
 namespace fp8g {
 
 struct LaunchArgs {
-    CUtensorMap tmap_a, tmap_b, tmap_d;
+    CUtensorMap tmap_a, tmap_b, tmap_d, tmap_sfa, tmap_sfb;
     Params p;
     int grid;
     cudaStream_t stream;
@@ -18,6 +18,10 @@ struct LaunchArgs {
 
 // Dynamic shared memory a launch with tiles of `block_n` columns needs.
 int smem_bytes_for(int block_n);
+
+// Width, in bf16 columns, of the output panels the kernel TMA-stores for
+// tiles of `block_n` columns (the D tensor map's box is 32 rows x this).
+int panel_cols_for(int block_n);
 
 cudaError_t launch_nt(int block_n, bool split, const LaunchArgs &a);
 cudaError_t launch_contiguous(int block_n, const LaunchArgs &a);

@@ -34,7 +34,7 @@ cudaError_t launch_one(const LaunchArgs &a)
     cfg.stream = a.stream;
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, kern, a.tmap_a, a.tmap_b, a.tmap_d, a.p);
+    return cudaLaunchKernelEx(&cfg, kern, a.tmap_a, a.tmap_b, a.tmap_d, a.tmap_sfa, a.tmap_sfb, a.p);
 }
 
 }  // namespace fp8g

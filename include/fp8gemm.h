@@ -29,7 +29,7 @@
  * Requirements (checked on the host before anything is launched):
  *   K % 128 == 0 and K > 0 (the kernel's BLOCK_K == 128 scaling contract);
  *   N % 16 == 0 (16-byte rows of D for the tensor-memory-access store);
- *   A, B, D, SFA 16-byte aligned; SFB 4-byte aligned;
+ *   A, B, D, SFA and SFB 16-byte aligned;
  *   contiguous: M_total % 128 == 0 (every 128-row block belongs to one group).
  *
  * Ownership and synchronisation: the caller owns every buffer.  Calls are

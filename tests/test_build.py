@@ -1,0 +1,54 @@
+"""Build checks that need no GPU: the register budget of every kernel.
+
+The kernel hands registers from its control warpgroup to its two epilogue
+warpgroups with setmaxnreg.  The request must fit the block's launch
+allocation (384 threads x the registers ptxas assigned at launch), or the
+epilogue's increase would wait forever; and no kernel should spill.
+"""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+KERNEL = os.path.join(ROOT, "fp8_block_scaled_persistent_gb300", "csrc", "gemm_kernel.cuh")
+
+
+def _const(name):
+    m = re.search(rf"constexpr int {name} = (\d+);", open(KERNEL).read())
+    assert m, name
+    return int(m.group(1))
+
+
+@pytest.fixture(scope="module")
+def ptxas_report():
+    from fp8_block_scaled_persistent_gb300 import build
+    build.build(force=not os.path.exists(build.PTXAS_LOG))
+    text = open(build.PTXAS_LOG).read()
+    entries = re.split(r"Compiling entry function '", text)[1:]
+    out = {}
+    for e in entries:
+        name = e.split("'")[0]
+        regs = int(re.search(r"Used (\d+) registers", e).group(1))
+        spill = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", e)
+        out[name] = (regs, int(spill.group(1)), int(spill.group(2)))
+    assert out, "no kernels in the ptxas report"
+    return out
+
+
+def test_register_reallocation_fits_the_launch_allocation(ptxas_report):
+    threads, ctl, epi, launch = (_const("kNumThreads"), _const("kRegsCtl"), _const("kRegsEpi"),
+                                 _const("kLaunchRegs"))
+    assert threads == 384
+    kernels = [n for n in ptxas_report if "fp8_gemm_kernel" in n]
+    assert len(kernels) == 7
+    for name in kernels:
+        regs = ptxas_report[name][0]
+        assert regs == launch, f"{name}: launched with {regs} registers, expected {launch}"
+        assert 128 * ctl + 256 * epi <= threads * regs, name
+        assert ctl % 8 == 0 and epi % 8 == 0 and 24 <= ctl <= epi <= 256
+
+
+def test_kernels_do_not_spill(ptxas_report):
+    for name, (_, st, ld) in ptxas_report.items():
+        assert st <= 64 and ld <= 64, f"{name}: {st} B spill stores, {ld} B spill loads"
