@@ -53,9 +53,33 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
         : "memory");
 }
 
+// One poll of the barrier phase.  FP8G_WAIT_MODE selects the form (a build
+// option for measurement): 0 = try_wait (may suspend the thread until the
+// phase completes or a system time limit passes), 1 = test_wait (never
+// suspends), 2 = try_wait with a 20 ns suspend-time hint.
+#ifndef FP8G_WAIT_MODE
+#define FP8G_WAIT_MODE 0
+#endif
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity)
 {
     uint32_t ok;
+#if FP8G_WAIT_MODE == 1
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+#elif FP8G_WAIT_MODE == 2
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity), "r"(20)
+        : "memory");
+#else
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -63,6 +87,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
         : "=r"(ok)
         : "r"(bar_addr), "r"(parity)
         : "memory");
+#endif
     return ok != 0;
 }
 
@@ -83,20 +108,22 @@ __device__ __forceinline__ void raise_abort(const WaitCtl &c)
 
 // Waits for the phase with the given parity to complete.  Returns false if the
 // wait ran out (the abort flag and the device error are then set) or if
-// another role of this CTA already aborted.
+// another role of this CTA already aborted.  The clock is only read after 32
+// failed polls, so a wait that succeeds quickly never touches it.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const WaitCtl &c)
 {
     const uint32_t a = smem_u32(bar);
-    if (mbar_try_wait(a, parity))
-        return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(a, parity))
             return true;
-        if ((it & 31u) == 0) {
+        if ((it & 31u) == 31u) {
             if (*c.abort_flag)
                 return false;
-            if (globaltimer_ns() - t0 > c.timeout_ns) {
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > c.timeout_ns) {
                 raise_abort(c);
                 return false;
             }
