@@ -327,17 +327,20 @@ def run_ours(args, dist, ws, rank, local):
 
 
 def load_traffic(name):
-    """dram bytes per launch from the committed ncu summary, when it still
-    describes the current kernel (profiles/traffic.json)."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch from the committed ncu summary
+    (profiles/traffic.txt), or None when it does not describe the current
+    kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    try:
-        with open(path) as f:
-            d = json.load(f)
-        return d.get(name)
-    except (OSError, ValueError):
-        return None
+    for line in open(path):
+        parts = line.split("#")[0].split()
+        if len(parts) == 2 and parts[0] == name:
+            try:
+                return float(parts[1])
+            except ValueError:
+                return None
+    return None
 
 
 # ----------------------------------------------------------------------------- CPU oracle
