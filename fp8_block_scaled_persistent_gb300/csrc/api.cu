@@ -165,38 +165,55 @@ struct NtChoice {
 };
 
 // Tile shape and schedule for a plain GEMM on a device with `sms` SMs.
-// workspace_bytes < 0 means "as much as it needs".
+// workspace_bytes < 0 means "as much as it needs".  With fewer output tiles
+// than SMs the K blocks of all tiles are shared evenly over the SMs (split-K)
+// with 128-column tiles (6 operand stages keep more of B in flight than the 3
+// of 256-column tiles; measured faster on small-M shapes), else 256-column
+// ones, whichever workspace fits first.
 int choose_nt(int M, int N, int K, int sms, long long workspace_bytes, NtChoice &c)
 {
     const int mb = ceil_div(M, 128);
-    const bool many = (long long)mb * ceil_div(N, 256) >= sms;
-    c.block_n = pick_block_n(N, many);
-    c.tiles = mb * ceil_div(N, c.block_n);
-    c.split_ctas = 0;
     const int kb = K / 128;
-    const int o = g_override_split.load();
+    const int obn = g_override_bn.load();
+    const int osplit = g_override_split.load();
+    auto tiles_for = [&](int bn) { return mb * ceil_div(N, bn); };
     // the kernel's split arithmetic is 32-bit: units * CTAs must stay below 2^31
-    const long long units = (long long)c.tiles * kb;
-    auto split_fits = [&](long long P) { return units * P < (1ll << 31); };
-    if (o > 0) {
-        if (c.block_n != 128)
-            return FP8G_ERR_INVALID_ARG;
-        const int P = (int)std::min<long long>(o, units);
-        if (!split_fits(P))
-            return FP8G_ERR_UNSUPPORTED;
-        if (workspace_bytes >= 0 && (long long)split_workspace_bytes(M, N, K, 128, P) > workspace_bytes)
-            return FP8G_ERR_WORKSPACE;
+    auto fits32 = [&](int bn, long long P) { return (long long)tiles_for(bn) * kb * P < (1ll << 31); };
+    auto bytes_ok = [&](int bn, long long P) {
+        return workspace_bytes < 0 || (long long)split_workspace_bytes(M, N, K, bn, (int)P) <= workspace_bytes;
+    };
+    auto set = [&](int bn, int P) {
+        c.block_n = bn;
+        c.tiles = tiles_for(bn);
         c.split_ctas = P;
-    } else if (o == 0 && c.block_n == 128 && c.tiles < sms && kb >= 8) {
-        // fewer output tiles than SMs: share the K blocks of all tiles evenly
-        // over the SMs, at least 4 K blocks per CTA
-        const long long P = std::min<long long>(sms, units / 4);
-        if (P > c.tiles && split_fits(P) &&
-            (workspace_bytes < 0 ||
-             (long long)split_workspace_bytes(M, N, K, 128, (int)P) <= workspace_bytes))
-            c.split_ctas = (int)P;
+        c.grid = P ? P : std::min(sms, c.tiles);
+    };
+    if (osplit > 0) {
+        const int bn = obn ? obn : 128;
+        const long long P = std::min<long long>(osplit, (long long)tiles_for(bn) * kb);
+        if (!fits32(bn, P))
+            return FP8G_ERR_UNSUPPORTED;
+        if (!bytes_ok(bn, P))
+            return FP8G_ERR_WORKSPACE;
+        set(bn, (int)P);
+        return FP8G_OK;
     }
-    c.grid = c.split_ctas ? c.split_ctas : std::min(sms, c.tiles);
+    if (osplit == 0 && kb >= 8) {
+        for (int bn : {128, 256}) {
+            if ((obn && bn != obn) || (bn == 256 && N <= 128))
+                continue;
+            const int t = tiles_for(bn);
+            if (t >= sms)
+                break;          // enough tiles to fill the SMs: no split
+            // at least 4 K blocks per CTA
+            const long long P = std::min<long long>(sms, (long long)t * kb / 4);
+            if (P > t && fits32(bn, P) && bytes_ok(bn, P)) {
+                set(bn, (int)P);
+                return FP8G_OK;
+            }
+        }
+    }
+    set(pick_block_n(N, (long long)mb * ceil_div(N, 256) >= sms), 0);
     return FP8G_OK;
 }
 
@@ -371,7 +388,7 @@ size_t fp8_gemm_workspace_size(int kind, int M, int N, int K, int G)
     NtChoice c;
     if (choose_nt(M, N, K, sms_or_default(), -1, c) != FP8G_OK || !c.split_ctas)
         return 0;
-    return split_workspace_bytes(M, N, K, 128, c.split_ctas);
+    return split_workspace_bytes(M, N, K, c.block_n, c.split_ctas);
 }
 
 size_t fp8_gemm_workspace_size_for(int M, int N, int K, int block_n, int split_ctas)
@@ -426,8 +443,6 @@ int fp8_gemm_sfa_ld(int M) { return M < 0 ? 0 : (M + 3) / 4 * 4; }
 int fp8_gemm_set_override(int block_n, int split_ctas)
 {
     if (block_n != 0 && block_n != 128 && block_n != 256)
-        return FP8G_ERR_INVALID_ARG;
-    if (split_ctas > 0 && block_n == 256)
         return FP8G_ERR_INVALID_ARG;
     g_override_bn.store(block_n);
     g_override_split.store(split_ctas);
@@ -502,13 +517,19 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const float *SFA, const void *
     if ((st = noalloc_scratch(dev_id, &scratch)) != FP8G_OK)
         return st;
 
-    // the same schedule fp8_gemm_nt picks when given all the workspace it asks for
+    // the schedule fp8_gemm_nt picks when given all the workspace it asks
+    // for, or, when that needs more than the static scratch, the best one
+    // that fits it; a forced split that does not fit is refused
     NtChoice c;
     if ((st = choose_nt(M, N, K, dev.sms, -1, c)) != FP8G_OK)
         return st;
+    if (c.split_ctas && split_workspace_bytes(M, N, K, c.block_n, c.split_ctas) > kNoAllocScratchBytes) {
+        if (g_override_split.load() > 0)
+            return FP8G_ERR_SCRATCH_LIMIT;
+        if ((st = choose_nt(M, N, K, dev.sms, (long long)kNoAllocScratchBytes, c)) != FP8G_OK)
+            return st;
+    }
     const size_t counters = ((size_t)c.tiles * 8 * sizeof(int) + 255) / 256 * 256;
-    if (c.split_ctas && split_workspace_bytes(M, N, K, 128, c.split_ctas) > kNoAllocScratchBytes)
-        return FP8G_ERR_SCRATCH_LIMIT;
 
     LaunchArgs a;
     fill_common(a.p, M, N, K, 1, SFA, SFB, D, nullptr, c.block_n, dev);

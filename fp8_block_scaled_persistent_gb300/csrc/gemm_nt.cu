@@ -17,7 +17,7 @@ int panel_cols_for(int block_n)
 cudaError_t launch_nt(int block_n, bool split, const LaunchArgs &a)
 {
     if (split)
-        return launch_one<128, kKindNT, true>(a);
+        return block_n == 256 ? launch_one<256, kKindNT, true>(a) : launch_one<128, kKindNT, true>(a);
     if (block_n == 256)
         return launch_one<256, kKindNT, false>(a);
     return launch_one<128, kKindNT, false>(a);

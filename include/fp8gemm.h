@@ -144,9 +144,9 @@ int fp8_gemm_sfa_ld(int M);
 /*
  * Tuning and test control (process-wide; 0 restores the automatic choice):
  *   block_n     : 128 or 256 columns per output tile;
- *   split_ctas  : > 0 forces the split-K schedule over that many CTAs (needs
- *                 a workspace of fp8_gemm_workspace_size_for bytes), < 0
- *                 forbids splitting.
+ *   split_ctas  : > 0 forces the split-K schedule over that many CTAs (with
+ *                 128-column tiles unless block_n says 256; needs a workspace
+ *                 of fp8_gemm_workspace_size_for bytes), < 0 forbids splitting.
  * Returns FP8G_ERR_INVALID_ARG for values outside those sets.
  */
 int fp8_gemm_set_override(int block_n, int split_ctas);

@@ -81,7 +81,7 @@ def test_grouped_validation(lib):
 
 def test_overrides_and_timeout_validation(lib):
     assert fg.fp8_gemm_set_override(100, 0) == fg.FP8G_ERR_INVALID_ARG
-    assert fg.fp8_gemm_set_override(256, 4) == fg.FP8G_ERR_INVALID_ARG
+    assert fg.fp8_gemm_set_override(256, 4) == fg.FP8G_OK
     assert fg.fp8_gemm_set_override(128, 4) == fg.FP8G_OK
     assert fg.fp8_gemm_set_override(0, 0) == fg.FP8G_OK
     assert fg.fp8_gemm_set_wait_timeout_ns(10) == fg.FP8G_ERR_INVALID_ARG
@@ -89,8 +89,9 @@ def test_overrides_and_timeout_validation(lib):
 
 
 def test_workspace_sizes_host_only(lib):
-    # small-M problems split K across SMs, large ones do not
-    assert fg.fp8_gemm_workspace_size(0, 128, 7168, 16384, 1) > 0
+    # small-M problems split K across SMs (128-column tiles), large ones do not
+    assert fg.fp8_gemm_workspace_size(0, 128, 7168, 16384, 1) == \
+        fg.fp8_gemm_workspace_size_for(128, 7168, 16384, 128, 152)
     assert fg.fp8_gemm_workspace_size(0, 4096, 7168, 2048, 1) == 0
     assert fg.fp8_gemm_workspace_size(1, 4096, 7168, 2048, 8) == 0
     n = fg.fp8_gemm_workspace_size_for(128, 256, 1024, 128, 10)

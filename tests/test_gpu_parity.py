@@ -92,33 +92,35 @@ def test_deterministic():
 
 # ------------------------------------------------------------------ split-K schedule
 
+@pytest.mark.parametrize("block_n", [128, 256])
 @pytest.mark.parametrize("M,N,K,P", [
     (64, 256, 2048, 7), (128, 512, 4096, 24), (100, 384, 1536, 5), (128, 128, 1024, 3),
     (64, 1024, 8192, 152), (1, 128, 512, 4)])
-def test_split_k_matches_oracle(M, N, K, P):
+def test_split_k_matches_oracle(M, N, K, P, block_n):
     import torch
     import fp8_block_scaled_persistent_gb300 as fg
-    assert fg.fp8_gemm_set_override(128, P) == 0
+    assert fg.fp8_gemm_set_override(block_n, P) == 0
     p = wl.make_nt(M, N, K, seed=M + K)
-    n = fg.fp8_gemm_workspace_size_for(M, N, K, 128, P)
+    n = fg.fp8_gemm_workspace_size_for(M, N, K, block_n, P)
     ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
     got, st, dst = gu.run(p, workspace=ws)
     assert st == 0 and dst == 0
-    check(got, _full_ref(p), f"split {M}x{N}x{K} P={P}")
+    check(got, _full_ref(p), f"split {M}x{N}x{K} P={P} bn{block_n}")
     # the tickets are back at zero, and a second run gives the same bits
-    ntiles = ((M + 127) // 128) * ((N + 127) // 128)
+    ntiles = ((M + 127) // 128) * ((N + block_n - 1) // block_n)
     assert int(ws[: ntiles * 8 * 4].view(torch.int32).abs().sum()) == 0
     again, st2, _ = gu.run(p, workspace=ws)
     assert st2 == 0 and np.array_equal(got, again)
 
 
-def test_split_k_exact_integers_bit_identical():
+@pytest.mark.parametrize("block_n", [128, 256])
+def test_split_k_exact_integers_bit_identical(block_n):
     import torch
     import fp8_block_scaled_persistent_gb300 as fg
     M, N, K, P = 128, 256, 3968, 9
-    assert fg.fp8_gemm_set_override(128, P) == 0
+    assert fg.fp8_gemm_set_override(block_n, P) == 0
     p = wl.exact_integer_problem(M, N, K, seed=5)
-    ws = torch.zeros(fg.fp8_gemm_workspace_size_for(M, N, K, 128, P), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(fg.fp8_gemm_workspace_size_for(M, N, K, block_n, P), dtype=torch.uint8, device="cuda")
     got, st, dst = gu.run(p, workspace=ws)
     assert st == 0 and dst == 0
     assert np.array_equal(got, _full_ref(p))
