@@ -116,6 +116,24 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t
                sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// An e4m3 operand [rows][K] viewed as [K/128][rows][128 B] (K-block stride
+// 128 bytes), with boxes of box_rows rows x 2 K blocks: one copy fills two
+// consecutive 128-byte-swizzled K-block tiles.
+bool make_pair_map(CUtensorMap *m, const void *base, uint64_t rows, int K, uint32_t box_rows)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    cuuint64_t dims[3] = {128, rows, (cuuint64_t)(K / 128)};
+    cuuint64_t strides[2] = {(cuuint64_t)K, 128};
+    cuuint32_t box[3] = {128, box_rows, 2};
+    cuuint32_t es[3] = {1, 1, 1};
+    std::memset(m, 0, sizeof(*m));
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------ validation
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -247,8 +265,9 @@ CUtensorMapSwizzle panel_swizzle(int cols)
 
 // Operand, output and scale views of one launch.  SFA is viewed as
 // [sfa_rows][sfa_ld] fp32 (sfa_rows = K/128, or G*K/128 when masked) and
-// loaded 128 rows' scales at a time; SFB as one flat fp32 vector of
-// G*ceil(N/128)*K/128 values, loaded in aligned groups of 4.
+// loaded 128 rows x kScaleChunk K blocks at a time; SFB as one flat fp32
+// vector of G*ceil(N/128)*K/128 values, loaded kScaleChunk + 4 at a time from
+// a 16-byte aligned start.
 bool make_maps(LaunchArgs &a, const void *A, const float *SFA, const void *B, const float *SFB, void *D,
                long long a_rows, long long b_rows, long long d_rows, long long sfa_rows, int sfa_ld,
                long long sfb_count, int N, int K, int block_n)
@@ -261,9 +280,12 @@ bool make_maps(LaunchArgs &a, const void *A, const float *SFA, const void *B, co
            make_map(&a.tmap_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, N, d_rows, (uint64_t)N * 2, pc, 32,
                     panel_swizzle(pc)) &&
            make_map(&a.tmap_sfa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SFA, sfa_ld, sfa_rows, (uint64_t)sfa_ld * 4,
-                    128, 1, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           make_map(&a.tmap_sfb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SFB, sfb_count, 0, 0, 4, 1,
-                    CU_TENSOR_MAP_SWIZZLE_NONE);
+                    128, fp8g::kScaleChunk, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           make_map(&a.tmap_sfb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SFB, sfb_count, 0, 0, fp8g::kScaleChunk + 4, 1,
+                    CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           (K < 256 ? (std::memset(&a.tmap_a2, 0, sizeof(a.tmap_a2)), std::memset(&a.tmap_b2, 0, sizeof(a.tmap_b2)), true)
+                    : (make_pair_map(&a.tmap_a2, A, (uint64_t)a_rows, K, 128) &&
+                       make_pair_map(&a.tmap_b2, B, (uint64_t)b_rows, K, (uint32_t)block_n)));
 }
 
 }  // namespace

@@ -10,10 +10,11 @@
 // "TCGen05 Copy Instruction" tutorial's warp-specialised matmul are prior art).
 // Three warpgroups of four warps:
 //   warp 0      TMA producer: 128x128 A and BNx128 B e4m3 tiles, 128-byte
-//               swizzled, into an S-stage shared-memory ring, and the K block's
-//               scales (128 A scales, the B scales of the tile's 128-column
-//               blocks) into a deeper scale ring.  mbarrier transaction counts
-//               signal completion.
+//               swizzled, into an S-stage shared-memory ring (with an even S,
+//               two K blocks per copy: one 3-D box fills two stages), and the
+//               scales of kScaleChunk K blocks at a time (128 A scales per K
+//               block, the B scales of the tile's 128-column blocks) into a
+//               scale ring.  mbarrier transaction counts signal completion.
 //   warp 1      MMA issuer: one thread issues 4 x tcgen05.mma kind::f8f6f4
 //               (128 x BN x 32) per K block into a FRESH tensor-memory buffer
 //               (the first MMA overwrites) and commits once per K block.  That
@@ -85,19 +86,26 @@ struct Cfg {
     static constexpr bool kFullTileStaging = BN == 256 && FP8G_FULL_TILE_STAGING != 0;
     static constexpr int kStages = (BN == 256) ? FP8G_STAGES_256 : 6;   // A/B operand ring
     static constexpr int kAccBufs = kTmemCols / BN;                     // TMEM partial buffers
-    static constexpr int kScaleSlots = kStages + kAccBufs;              // scale ring: never the limiter
+    static constexpr int kScaleSlots = 4;                               // scale chunk ring
     static constexpr int kABytes = kBM * kBK;                           // e4m3
     static constexpr int kBBytes = BN * kBK;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kSfbRows = BN / 128;                           // 128-column blocks per tile
-    // scale slot: 128 A scales (one per tile row), then per column block a
-    // 16-byte group of 4 consecutive B scales that holds this K block's one.
+    // scale slot (one chunk of kScaleChunk K blocks): the A scales as
+    // [kScaleChunk][128 rows], then per column block the kScaleChunk + 4 B
+    // scales from the 16-byte aligned group that holds the chunk's first one.
     // Every TMA destination in shared memory starts on a 128-byte boundary.
-    static constexpr int kSlotSfaBytes = kBM * 4;
+    static constexpr int kSlotSfaBytes = kScaleChunk * kBM * 4;
     static constexpr int kSlotSfbStride = 128;
     static constexpr int kSlotBytes = kSlotSfaBytes + kSlotSfbStride * kSfbRows;
-    static constexpr int kSlotTxBytes = kSlotSfaBytes + 16 * kSfbRows;
+    static constexpr int kSlotTxBytes = kSlotSfaBytes + (kScaleChunk + 4) * 4 * kSfbRows;
+    static_assert((kScaleChunk + 4) * 4 <= kSlotSfbStride && (kScaleChunk + 4) % 4 == 0, "B scale box");
     static constexpr int kColsPerThread = BN / 2;
+    // Pair loads: one 3-D copy per operand fills two consecutive stages with
+    // two consecutive K blocks of the same tile (fewer, larger copies for the
+    // SM's TMA unit).  Pairs start at even stages only, hence an even stage
+    // count.
+    static constexpr bool kPairLoads = kStages % 2 == 0;
     // output panels: 32 rows x kPanelCols bf16, TMA-stored with the swizzle
     // of their row width
     static constexpr int kPanelCols = kFullTileStaging ? FP8G_PANEL_COLS_FULL : 16;
@@ -363,7 +371,8 @@ template <int BN, int KIND, bool SPLIT>
 __global__ void __launch_bounds__(kNumThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_sfa,
-                    const __grid_constant__ CUtensorMap tmap_sfb, const __grid_constant__ Params p)
+                    const __grid_constant__ CUtensorMap tmap_sfb, const __grid_constant__ CUtensorMap tmap_a2,
+                    const __grid_constant__ CUtensorMap tmap_b2, const __grid_constant__ Params p)
 {
 #if defined(__CUDA_ARCH__)
     using C = Cfg<BN>;
@@ -414,6 +423,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         prefetch_tensormap(&tmap_d);
         prefetch_tensormap(&tmap_sfa);
         prefetch_tensormap(&tmap_sfb);
+        if (C::kPairLoads && p.kb >= 2) {
+            prefetch_tensormap(&tmap_a2);
+            prefetch_tensormap(&tmap_b2);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
@@ -436,33 +449,63 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             Work w;
             Ring ring, sring;
             uint32_t issued = 0, issued_parity = 0, sissued = 0, sissued_parity = 0;
+            bool second = false;    // this K block's operands came with the previous block's
             bool ok = true;
             while (ok && sched.next(w)) {
                 const int b_row0 = w.g * p.N + w.n_blk * BN;
                 const int sfa_y0 = (KIND == kKindMasked) ? w.g * p.kb : 0;
                 const int sfb_x0 = (w.g * p.nb + (w.n_blk * BN) / 128) * p.kb;
                 for (int k = w.kb0; k < w.kb1; ++k) {
-                    if (!mbar_wait(&empty[ring.i], ring.ph ^ 1u, ctl) ||
-                        !mbar_wait(&sempty[sring.i], sring.ph ^ 1u, ctl)) {
-                        ok = false;
-                        break;
+                    if (!second) {
+                        // a pair starts on an even stage and needs the next K
+                        // block in the same work unit
+                        const bool pair = C::kPairLoads && (ring.i & 1u) == 0 && k + 1 < w.kb1;
+                        if (!mbar_wait(&empty[ring.i], ring.ph ^ 1u, ctl) ||
+                            (pair && !mbar_wait(&empty[ring.i + 1], ring.ph ^ 1u, ctl))) {
+                            ok = false;
+                            break;
+                        }
+                        if (pair) {
+                            // both tiles signal the first stage's barrier; the
+                            // second stage's barrier completes its phase with a
+                            // plain arrival, so that every barrier keeps one
+                            // phase per use of its stage (the MMA warp does not
+                            // wait on it: it waited on the first one)
+                            mbar_arrive_expect_tx(&full[ring.i], 2 * C::kStageBytes);
+                            tma_load_3d(sm_a + ring.i * C::kABytes, &tmap_a2, &full[ring.i], 0, w.a_row0, k);
+                            tma_load_3d(sm_b + ring.i * C::kBBytes, &tmap_b2, &full[ring.i], 0, b_row0, k);
+                            mbar_arrive(&full[ring.i + 1]);
+                            issued |= 2u << ring.i;
+                            issued_parity = (issued_parity & ~(2u << ring.i)) | (ring.ph << (ring.i + 1));
+                        } else {
+                            mbar_arrive_expect_tx(&full[ring.i], C::kStageBytes);
+                            tma_load_2d(sm_a + ring.i * C::kABytes, &tmap_a, &full[ring.i], k * kBK, w.a_row0);
+                            tma_load_2d(sm_b + ring.i * C::kBBytes, &tmap_b, &full[ring.i], k * kBK, b_row0);
+                        }
+                        issued |= 1u << ring.i;
+                        issued_parity = (issued_parity & ~(1u << ring.i)) | (ring.ph << ring.i);
+                        second = pair;
+                    } else {
+                        second = false;
                     }
-                    mbar_arrive_expect_tx(&full[ring.i], C::kStageBytes);
-                    tma_load_2d(sm_a + ring.i * C::kABytes, &tmap_a, &full[ring.i], k * kBK, w.a_row0);
-                    tma_load_2d(sm_b + ring.i * C::kBBytes, &tmap_b, &full[ring.i], k * kBK, b_row0);
-                    uint8_t *slot = sm_scales + sring.i * C::kSlotBytes;
-                    mbar_arrive_expect_tx(&sfull[sring.i], C::kSlotTxBytes);
-                    tma_load_2d(slot, &tmap_sfa, &sfull[sring.i], w.m_blk * kBM, sfa_y0 + k);
+                    if ((k - w.kb0) % kScaleChunk == 0) {
+                        // the scales of the chunk of K blocks starting here
+                        if (!mbar_wait(&sempty[sring.i], sring.ph ^ 1u, ctl)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t *slot = sm_scales + sring.i * C::kSlotBytes;
+                        mbar_arrive_expect_tx(&sfull[sring.i], C::kSlotTxBytes);
+                        tma_load_2d(slot, &tmap_sfa, &sfull[sring.i], w.m_blk * kBM, sfa_y0 + k);
 #pragma unroll
-                    for (int j = 0; j < C::kSfbRows; ++j)
-                        tma_load_1d(slot + C::kSlotSfaBytes + C::kSlotSfbStride * j, &tmap_sfb, &sfull[sring.i],
-                                    (sfb_x0 + j * p.kb + k) & ~3);
-                    issued |= 1u << ring.i;
-                    issued_parity = (issued_parity & ~(1u << ring.i)) | (ring.ph << ring.i);
-                    sissued |= 1u << sring.i;
-                    sissued_parity = (sissued_parity & ~(1u << sring.i)) | (sring.ph << sring.i);
+                        for (int j = 0; j < C::kSfbRows; ++j)
+                            tma_load_1d(slot + C::kSlotSfaBytes + C::kSlotSfbStride * j, &tmap_sfb,
+                                        &sfull[sring.i], (sfb_x0 + j * p.kb + k) & ~3);
+                        sissued |= 1u << sring.i;
+                        sissued_parity = (sissued_parity & ~(1u << sring.i)) | (sring.ph << sring.i);
+                        sring.template next<SR>();
+                    }
                     ring.template next<S>();
-                    sring.template next<SR>();
                 }
             }
             // every fill this thread started has landed before the CTA exits
@@ -478,10 +521,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             Work w;
             Ring ring, acc;
             constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
+            bool second = false;    // this K block's operands came with the previous block's
             bool ok = true;
             while (ok && sched.next(w)) {
                 for (int k = w.kb0; k < w.kb1; ++k) {
-                    if (!mbar_wait(&tempty[acc.i], acc.ph ^ 1u, ctl) || !mbar_wait(&full[ring.i], ring.ph, ctl)) {
+                    // the producer's pairing rule
+                    const bool pair = !second && C::kPairLoads && (ring.i & 1u) == 0 && k + 1 < w.kb1;
+                    if (!mbar_wait(&tempty[acc.i], acc.ph ^ 1u, ctl) ||
+                        (!second && !mbar_wait(&full[ring.i], ring.ph, ctl))) {
                         ok = false;
                         break;
                     }
@@ -496,6 +543,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     // pipe): it frees the operand stage for the producer and
                     // tells the epilogue that TMEM buffer acc.i is complete.
                     mma_commit(&empty[ring.i]);
+                    second = pair;
                     ring.template next<S>();
                     acc.template next<NACC>();
                 }
@@ -539,10 +587,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 // up to S + NACC blocks ahead), then its MMA completion.  The
                 // stage barrier cannot have moved on: MMA k+S needs the TMEM
                 // buffer this warp frees after block k+S-NACC >= k.
+                const int kc = (k - w.kb0) % kScaleChunk;     // position in the scale chunk
+                const int k0 = k - kc;
                 int got = 1;
                 if (lane == 0)
-                    got = (mbar_wait(&sfull[sring.i], sring.ph, ctl) && mbar_wait(&empty[ring.i], ring.ph, ctl)) ? 1
-                                                                                                               : 0;
+                    got = ((kc != 0 || mbar_wait(&sfull[sring.i], sring.ph, ctl)) &&
+                           mbar_wait(&empty[ring.i], ring.ph, ctl))
+                              ? 1
+                              : 0;
                 got = __shfl_sync(0xffffffffu, got, 0);
                 if (!got) {
                     ok = false;
@@ -551,17 +603,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 __syncwarp();           // orders lane 0's barrier waits before every lane's reads
                 tc_fence_after_sync();
                 const uint8_t *slot = sm_scales + sring.i * C::kSlotBytes;
-                const float sa = reinterpret_cast<const float *>(slot)[row_in_tile];
-                // the slot holds the aligned group of 4 around this K block's
-                // B scale: its flat index in SFB picks the element
-                const int sfb_idx = (w.g * p.nb + (w.n_blk * BN) / 128 + sfb_row) * p.kb + k;
-                const float sb =
-                    reinterpret_cast<const float *>(slot + C::kSlotSfaBytes + C::kSlotSfbStride * sfb_row)[sfb_idx & 3];
+                const float sa = reinterpret_cast<const float *>(slot)[kc * kBM + row_in_tile];
+                // the B part starts at the aligned group of 4 that holds the
+                // chunk's first B scale: the flat SFB index picks the element
+                const int sfb_idx0 = (w.g * p.nb + (w.n_blk * BN) / 128 + sfb_row) * p.kb + k0;
+                const float sb = reinterpret_cast<const float *>(slot + C::kSlotSfaBytes +
+                                                                 C::kSlotSfbStride * sfb_row)[(sfb_idx0 & 3) + kc];
                 const float s = sa * sb;
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&sempty[sring.i]);
-                sring.template next<SR>();
+                if (kc == kScaleChunk - 1 || k + 1 == w.kb1) {
+                    // last K block of the chunk: the slot may be refilled
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&sempty[sring.i]);
+                    sring.template next<SR>();
+                }
 
                 const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + acc_ring.i * BN + h * COLS;
                 promote_block<COLS, 64>(acc, taddr, s, &tempty[acc_ring.i], lane);

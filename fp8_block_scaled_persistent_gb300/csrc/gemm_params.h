@@ -8,6 +8,12 @@ namespace fp8g {
 // Bits of the sticky device-side error word.
 enum : int { kErrTimeoutBit = 1, kErrBadGroupBit = 2 };
 
+// K blocks whose scales one scale copy brings in: the A scales of 128 rows x
+// kScaleChunk K blocks (one 2-D box) and, per 128-column block, the B scales
+// of those K blocks (one 1-D box of kScaleChunk + 4 values from the 16-byte
+// aligned start).  Chunks start at each work unit's first K block.
+constexpr int kScaleChunk = 8;
+
 struct Params {
     int rows;          // NT: M, contiguous: M_total, masked: M_max
     int N, K, G;

@@ -11,6 +11,9 @@ namespace fp8g {
 
 struct LaunchArgs {
     CUtensorMap tmap_a, tmap_b, tmap_d, tmap_sfa, tmap_sfb;
+    // A and B viewed as [K/128][rows][128 B] with boxes two K blocks deep
+    // (zeroed, and never used, when K/128 < 2)
+    CUtensorMap tmap_a2, tmap_b2;
     Params p;
     int grid;
     cudaStream_t stream;

@@ -1,5 +1,5 @@
 // launch_impl.cuh -- one launch of a kernel instantiation (persistent grid,
-// 320 threads, the configuration's dynamic shared memory).
+// kNumThreads threads, the configuration's dynamic shared memory).
 #pragma once
 
 #include <atomic>
@@ -34,7 +34,8 @@ cudaError_t launch_one(const LaunchArgs &a)
     cfg.stream = a.stream;
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, kern, a.tmap_a, a.tmap_b, a.tmap_d, a.tmap_sfa, a.tmap_sfb, a.p);
+    return cudaLaunchKernelEx(&cfg, kern, a.tmap_a, a.tmap_b, a.tmap_d, a.tmap_sfa, a.tmap_sfb, a.tmap_a2, a.tmap_b2,
+                              a.p);
 }
 
 }  // namespace fp8g
