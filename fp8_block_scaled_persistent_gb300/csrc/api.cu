@@ -487,14 +487,14 @@ int fp8_gemm_version(void) { return kVersion; }
 // fp8_gemm_nt_noalloc: the plain GEMM for callers that cannot call cudaMalloc
 // (code running inside an allocator callback, plug-ins whose host framework
 // owns all device memory, loops that forbid allocation after start-up) and so
-// cannot hand over a workspace.  The split-K schedule's scratch (ticket
+// cannot hand over a workspace.  The split-K schedule's scratch (counter
 // counters and fp32 partials) lives in the static array below instead.
 
 namespace {
 
 // Largest scratch the split-K schedule may use through fp8_gemm_nt_noalloc.
 // It covers the schedule fp8_gemm_nt picks for any plain GEMM on a GPU with
-// up to 190 SMs (2 fp32 slots of 128 x 128 per CTA plus the tickets).
+// up to 190 SMs (2 fp32 slots of 128 x 128 per CTA plus the counters).
 constexpr size_t kNoAllocScratchBytes = size_t(24) << 20;
 
 // Every GPU that loads this library holds this array until the process exits.
@@ -563,7 +563,7 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const float *SFA, const void *
         a.p.units = c.tiles * a.p.kb;
         a.p.counters = static_cast<int *>(scratch);
         a.p.partials = reinterpret_cast<float *>(static_cast<char *>(scratch) + counters);
-        // the array keeps the previous call's contents: the tickets start at zero
+        // the array keeps the previous call's contents: the counters start at zero
         if (cudaMemsetAsync(scratch, 0, counters, a.stream) != cudaSuccess)
             return FP8G_ERR_CUDA;
     }

@@ -34,8 +34,8 @@
 //               rasterisation (m fastest inside a band of m-blocks); grouped
 //               layouts map tiles to groups.  A split-K ("stream-K") variant
 //               gives each CTA an equal share of the (tile, K-block) units and
-//               lets the last contributor of each tile reduce the fp32
-//               partials in a fixed order (deterministic, no spin-wait).
+//               lets the highest contributor of each tile reduce the fp32
+//               partials in a fixed order (deterministic).
 //
 // Every wait is bounded (see ptx.cuh); on expiry a CTA records an error,
 // drains its copies in flight, frees its tensor memory and returns.
@@ -187,12 +187,16 @@ struct Scheduler {
     __device__ bool next(Work &w)
     {
         if constexpr (SPLIT) {
+            // the CTA's units [u, u_end) are taken tile by tile from the END
+            // of the range: a tile's highest contributor then works on its
+            // share of the tile last, like every other contributor, and can
+            // be the one that reduces the tile
             if (u >= u_end)
                 return false;
-            const int t = u / p.kb;
-            const int k0 = u - t * p.kb;
-            const int k1 = min(p.kb, k0 + (u_end - u));
-            u += k1 - k0;
+            const int t = (u_end - 1) / p.kb;
+            const int k1 = u_end - t * p.kb;
+            const int k0 = max(0, u - t * p.kb);
+            u_end = t * p.kb + k0;
             raster(t, p.num_m_blocks, p.num_n_blocks, p.group_m, w.m_blk, w.n_blk);
             w.g = 0;
             w.tile = t;
@@ -626,11 +630,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (!ok)
                 break;
 
+            bool has_out = true;
             if constexpr (SPLIT) {
                 if (!(w.kb0 == 0 && w.kb1 == p.kb)) {
-                    // split tile: publish this CTA's partial for this warp's
-                    // 32 x COLS region, take a ticket; the last contributor
-                    // sums all partials in CTA order and stores the tile.
+                    // split tile: contributors c_lo .. c_hi (CTA order) each
+                    // hold the partial of their K range.  All but c_hi publish
+                    // theirs for this warp's 32 x COLS region and bump the
+                    // region's counter; c_hi (which works on its share last)
+                    // waits for the counter, sums the published partials in CTA
+                    // order, adds its own and stores the tile.
                     const int t = w.tile;
                     const int P = gridDim.x;
                     const int c_lo = unit_owner(t * p.kb, p.units, P);
@@ -644,47 +652,50 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         return reinterpret_cast<float4 *>(p.partials) +
                                ((size_t)slot_of(c) * kNumEpiWarps + ew) * F4 * 32;
                     };
-                    float4 *mine = region(blockIdx.x);
-#pragma unroll
-                    for (int j = 0; j < F4; ++j)
-                        st_cg_f4(mine + j * 32 + lane,
-                                 make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
-                    __threadfence();
-                    __syncwarp();
-                    int ticket = 0;
                     int *ctr = p.counters + (size_t)t * kNumEpiWarps + ew;
-                    if (lane == 0) {
+                    if ((int)blockIdx.x != c_hi) {
+                        float4 *mine = region(blockIdx.x);
+#pragma unroll
+                        for (int j = 0; j < F4; ++j)
+                            st_cg_f4(mine + j * 32 + lane,
+                                     make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
                         __threadfence();
-                        ticket = atomicAdd(ctr, 1);
-                    }
-                    ticket = __shfl_sync(0xffffffffu, ticket, 0);
-                    if (ticket != c_hi - c_lo)
-                        continue;       // not the last contributor
-                    __threadfence();
-                    // every partial, this CTA's included, is summed back from
-                    // L2 in CTA order, so the result does not depend on which
-                    // contributor arrived last
-#pragma unroll
-                    for (int i = 0; i < COLS; ++i)
-                        acc[i] = 0.f;
-                    for (int c = c_lo; c <= c_hi; ++c) {
-                        const float4 *src = region(c);
-#pragma unroll
-                        for (int j = 0; j < F4; ++j) {
-                            const float4 v = ld_cg_f4(src + j * 32 + lane);
-                            acc[4 * j] += v.x;
-                            acc[4 * j + 1] += v.y;
-                            acc[4 * j + 2] += v.z;
-                            acc[4 * j + 3] += v.w;
+                        __syncwarp();
+                        if (lane == 0)
+                            red_release_add(ctr, 1);
+                        has_out = false;
+                    } else {
+                        int got = 1;
+                        if (lane == 0)
+                            got = wait_counter(ctr, c_hi - c_lo, ctl) ? 1 : 0;
+                        got = __shfl_sync(0xffffffffu, got, 0);
+                        if (!got) {
+                            ok = false;
+                            break;
                         }
+                        __threadfence();
+                        // this CTA's partial, then the published ones in CTA
+                        // order: one fixed sequence of additions per tile,
+                        // however the contributors' timing falls
+                        for (int c = c_lo; c < c_hi; ++c) {
+                            const float4 *src = region(c);
+#pragma unroll
+                            for (int j = 0; j < F4; ++j) {
+                                const float4 v = ld_cg_f4(src + j * 32 + lane);
+                                acc[4 * j] += v.x;
+                                acc[4 * j + 1] += v.y;
+                                acc[4 * j + 2] += v.z;
+                                acc[4 * j + 3] += v.w;
+                            }
+                        }
+                        if (lane == 0)
+                            *ctr = 0;   // leave the workspace zeroed for the next call
                     }
-                    if (lane == 0)
-                        *ctr = 0;       // leave the workspace zeroed for the next call
                 }
             }
 
             // ---- bf16 store of this warp's 32 rows x COLS columns
-            const int rows_ok = min(max(w.valid_rows - 32 * q, 0), 32);
+            const int rows_ok = has_out ? min(max(w.valid_rows - 32 * q, 0), 32) : 0;
             const int y_row0 = w.a_row0 + 32 * q;
             if constexpr (C::kFullTileStaging) {
                 // the previous tile's stores have had a whole tile to read

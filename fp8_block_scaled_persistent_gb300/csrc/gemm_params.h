@@ -29,7 +29,7 @@ struct Params {
     int num_tiles;     // NT and contiguous
     int units;         // split: num_tiles * kb (the host keeps units * CTAs < 2^31)
     float *partials;   // split: 2 * gridDim.x slots of 128 x BN fp32
-    int *counters;     // split: num_tiles * 8 tickets
+    int *counters;     // split: num_tiles * 8 counters of published partials
     int *error_word;
     unsigned long long timeout_ns;
 };

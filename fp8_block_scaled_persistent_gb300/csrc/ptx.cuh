@@ -436,6 +436,44 @@ __device__ __forceinline__ float ld_nc_f32(const float *p)
     return v;
 }
 
+// Release-ordered atomic add whose result is not needed (a reduction).
+__device__ __forceinline__ void red_release_add(int *p, int v)
+{
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits until *ctr (bumped by other CTAs of the same grid) reaches `target`.
+// Every CTA of the persistent grid is resident, so the wait ends unless a
+// contributor failed; it is bounded like every other wait.  Returns false on
+// expiry or abort (the error is recorded).
+__device__ __forceinline__ bool wait_counter(const int *ctr, int target, const WaitCtl &c)
+{
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (ld_acquire(ctr) >= target)
+            return true;
+        __nanosleep(100);
+        if ((it & 15u) == 15u) {
+            if (*c.abort_flag)
+                return false;
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > c.timeout_ns) {
+                raise_abort(c);
+                return false;
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ float4 ld_cg_f4(const float4 *p)
 {
     float4 v;

@@ -173,7 +173,7 @@ int fp8_gemm_set_wait_timeout_ns(uint64_t ns);
  *
  * Same operation, layouts, requirements and schedule as fp8_gemm_nt given
  * all the workspace it asks for; the caller still passes A, SFA, B, SFB and
- * D.  The split-K scratch (tickets and fp32 partials) is a static device
+ * D.  The split-K scratch (counters and fp32 partials) is a static device
  * array of 24 MiB (25,165,824 bytes) inside this library, enough for the
  * schedule of any plain GEMM on a GPU with up to 190 SMs; every GPU that
  * loads the library holds it until the process exits.  Nothing is allocated per call: no cudaMalloc, no cudaFree.
@@ -182,7 +182,7 @@ int fp8_gemm_set_wait_timeout_ns(uint64_t ns);
  *     that first call before any stream capture.
  *   - A problem whose split-K schedule needs more scratch than the array
  *     holds returns FP8G_ERR_SCRATCH_LIMIT and launches nothing.
- *   - Every call shares the one array and clears its tickets (an async
+ *   - Every call shares the one array and clears its counters (an async
  *     memset on `stream`) before launching; calls that overlap on the GPU
  *     (different streams, or several host threads) race on it and must be
  *     serialised by the caller.
