@@ -440,6 +440,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Launched as a programmatic dependent of the previous kernel on the
+    // stream, the set-up above (barriers, tensor memory, descriptor prefetch)
+    // may overlap that kernel's tail; nothing in global memory is touched
+    // before the previous grid has completed and its writes are visible.  The
+    // next kernel may then be scheduled as SMs free up.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     const WaitCtl ctl{abort_flag, p.error_word, p.timeout_ns};
 

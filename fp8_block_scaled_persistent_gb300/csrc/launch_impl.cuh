@@ -5,6 +5,10 @@
 #include <atomic>
 
 #include "gemm_kernel.cuh"
+
+#ifndef FP8G_PDL
+#define FP8G_PDL 1
+#endif
 #include "launch.h"
 
 namespace fp8g {
@@ -32,8 +36,14 @@ cudaError_t launch_one(const LaunchArgs &a)
     cfg.blockDim = dim3(kNumThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = a.stream;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
+    // programmatic stream serialisation: the kernel may be scheduled while the
+    // previous kernel on the stream finishes; it waits (griddepcontrol.wait)
+    // before it reads or writes global memory
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = FP8G_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, a.tmap_a, a.tmap_b, a.tmap_d, a.tmap_sfa, a.tmap_sfb, a.tmap_a2, a.tmap_b2,
                               a.p);
 }

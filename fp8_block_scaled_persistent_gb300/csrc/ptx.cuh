@@ -145,6 +145,23 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, 
     }
 }
 
+// ---------------------------------------------------------------- grid dependencies
+
+// Waits until the grids this one depends on (programmatic stream
+// serialisation) have completed and their memory is visible; a no-op for a
+// grid launched without that attribute.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the grids that depend on this one be scheduled (they still wait for
+// this grid's completion before they touch memory).
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- fences
 
 __device__ __forceinline__ void fence_proxy_async_shared()
