@@ -191,9 +191,11 @@ class GemmCase:
         self.ws = gu.workspace_for(self.p, device)
         self.flops = self.p.flops()
         self.bytes = self.p.algorithmic_bytes()
-        # pinned host copies for the end-to-end measurement
+        # pinned host copies for the end-to-end measurement; two device input
+        # sets (copies 0 and 1) and two outputs let consecutive steps overlap
         self.host = {k: v.cpu().pin_memory() for k, v in self.t.items()}
-        self.D_host = torch.empty(self.D.shape, dtype=self.D.dtype).pin_memory()
+        self.D_host = [torch.empty(self.D.shape, dtype=self.D.dtype).pin_memory() for _ in range(2)]
+        self.D2 = [self.D, torch.empty_like(self.D)]
         self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.host.values())
         self.d2h_bytes = self.D.numel() * self.D.element_size()
         if dist_rank == 0:
@@ -203,13 +205,18 @@ class GemmCase:
         from tests import gpu_util as gu
         return gu.call(self.p, self.sets[step % self.copies], self.D, workspace=self.ws, stream=stream)
 
-    def e2e(self, stream):
-        """H2D of the inputs from pinned memory, the GEMM, D2H of D."""
+    def e2e_h2d(self, buf):
+        """Host -> device copies of the inputs into device set `buf` (0 or 1)."""
         for k, v in self.host.items():
-            self.t[k].copy_(v, non_blocking=True)
-        st = self.launch(stream)
-        self.D_host.copy_(self.D, non_blocking=True)
-        return st
+            self.sets[buf][k].copy_(v, non_blocking=True)
+
+    def e2e_gemm(self, buf, stream):
+        from tests import gpu_util as gu
+        return gu.call(self.p, self.sets[buf], self.D2[buf], workspace=self.ws, stream=stream)
+
+    def e2e_d2h(self, buf):
+        """Device -> host copy of output buffer `buf` into pinned memory."""
+        self.D_host[buf].copy_(self.D2[buf], non_blocking=True)
 
 
 def run_ours(args, dist, ws, rank, local):
@@ -281,22 +288,54 @@ def run_ours(args, dist, ws, rank, local):
     bytes_step = sum(c.bytes for c in cases)
     value = sum_over_ranks(dist, flops_step * args.steps, device) / (total_ms / 1e3) / 1e12
 
-    # end-to-end through the C ABI with host buffers (pinned), copies timed
-    e2e_steps = max(3, min(50, args.steps // 20))
-    for _ in range(2):
-        for c in cases:
-            c.e2e(stream)
+    # end-to-end through the C ABI with host buffers (pinned), copies timed.
+    # Three streams: inputs in, GEMMs, result out; step s uses device buffer
+    # s % 2, so step s+1's inputs travel while step s computes and step s-1's
+    # result travels back.  Events keep a buffer from being refilled before
+    # its GEMM has read it and an output from being overwritten before it has
+    # been copied out.
+    e2e_steps = max(4, min(50, args.steps // 20))
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    s_gemm = stream
+
+    def e2e_run(nsteps):
+        consumed = [[None, None] for _ in cases]    # GEMM done with input buffer
+        copied = [[None, None] for _ in cases]      # output buffer copied out
+        for st_i in range(nsteps):
+            buf = st_i % 2
+            for i, c in enumerate(cases):
+                with torch.cuda.stream(s_in):
+                    if consumed[i][buf] is not None:
+                        s_in.wait_event(consumed[i][buf])
+                    c.e2e_h2d(buf)
+                    ready = torch.cuda.Event()
+                    ready.record(s_in)
+                s_gemm.wait_event(ready)
+                if copied[i][buf] is not None:
+                    s_gemm.wait_event(copied[i][buf])
+                rc = c.e2e_gemm(buf, s_gemm)
+                if rc != 0:
+                    raise fg.Fp8GemmError(rc, c.name)
+                done = torch.cuda.Event()
+                done.record(s_gemm)
+                consumed[i][buf] = done
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(done)
+                    c.e2e_d2h(buf)
+                    out = torch.cuda.Event()
+                    out.record(s_out)
+                copied[i][buf] = out
+
+    e2e_run(2)
     torch.cuda.synchronize()
     barrier(dist)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        for c in cases:
-            st = c.e2e(stream)
-            if st != 0:
-                raise fg.Fp8GemmError(st, c.name)
-    e1.record(stream)
+    e0.record(s_gemm)
+    s_in.wait_event(e0)
+    e2e_run(e2e_steps)
+    s_gemm.wait_stream(s_out)
+    e1.record(s_gemm)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1), device)
     e2e_value = sum_over_ranks(dist, flops_step * e2e_steps, device) / (e2e_ms / 1e3) / 1e12
@@ -344,7 +383,8 @@ def run_ours(args, dist, ws, rank, local):
         "shapes": shapes, "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": sum(c.h2d_bytes for c in cases),
-                "d2h_bytes_per_step": sum(c.d2h_bytes for c in cases), "steps": e2e_steps},
+                "d2h_bytes_per_step": sum(c.d2h_bytes for c in cases), "steps": e2e_steps,
+                "overlap": "3 streams (inputs in, GEMMs, result out), double-buffered across steps"},
         "gpu_launches": len(cases) * args.steps,
         "clocks": clocks, "wall_s_timed_region": wall, "impl": "ours",
     }
