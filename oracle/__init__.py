@@ -61,6 +61,9 @@ def _bind(lib):
     lib.oracle_gemm_nt_rows.restype = None
     lib.oracle_gemm_nt_rows.argtypes = [u8p, f32p, u8p, f32p, I, I, I,
                                         i32p, I, u16p, f64p]
+    lib.oracle_gemm_nt_acc_rows.restype = None
+    lib.oracle_gemm_nt_acc_rows.argtypes = [u8p, f32p, u8p, f32p, f32p, I, I, I,
+                                            i32p, I, u16p, f64p]
     lib.oracle_gemm_grouped_contiguous_rows.restype = None
     lib.oracle_gemm_grouped_contiguous_rows.argtypes = [
         u8p, f32p, u8p, f32p, i32p, I, I, I, I, i32p, I, u16p]
@@ -175,6 +178,28 @@ def gemm_nt_rows(A, SFA, B, SFB, M, N, K, rows, threads=1, want_acc=False, lib=N
         lib.oracle_gemm_nt_rows(
             _ptr(A, ctypes.c_uint8), _ptr(SFA, ctypes.c_float),
             _ptr(B, ctypes.c_uint8), _ptr(SFB, ctypes.c_float), M, N, K,
+            _ptr(chunk, ctypes.c_int), len(chunk),
+            _ptr(D[chunk_start:], ctypes.c_uint16),
+            _ptr(acc[chunk_start:], ctypes.c_double) if want_acc else None)
+
+    _run_chunks(rows, threads, run)
+    return (D, acc) if want_acc else D
+
+
+def gemm_nt_acc_rows(A, SFA, B, SFB, C, M, N, K, rows, threads=1, want_acc=False, lib=None):
+    """Rows ``rows`` of the plain product plus the fp32 addend ``C`` [M][N]."""
+    lib = lib or _load()
+    A, B, SFA, SFB, C = _u8(A), _u8(B), _f32(SFA), _f32(SFB), _f32(C)
+    assert C.size == M * N, "C must be [M][N]"
+    rows = _i32(rows)
+    D = np.empty((len(rows), N), np.uint16)
+    acc = np.empty((len(rows), N), np.float64) if want_acc else None
+
+    def run(chunk_start, chunk):
+        lib.oracle_gemm_nt_acc_rows(
+            _ptr(A, ctypes.c_uint8), _ptr(SFA, ctypes.c_float),
+            _ptr(B, ctypes.c_uint8), _ptr(SFB, ctypes.c_float),
+            _ptr(C, ctypes.c_float), M, N, K,
             _ptr(chunk, ctypes.c_int), len(chunk),
             _ptr(D[chunk_start:], ctypes.c_uint16),
             _ptr(acc[chunk_start:], ctypes.c_double) if want_acc else None)

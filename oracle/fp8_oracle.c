@@ -14,6 +14,10 @@
  *   acc(m,n)  = sum_{k=0}^{K/128-1} (SFA[k][m] * SFB[n/128][k]) * S_k(m,n)
  *   D(m,n)    = bf16_rne(acc(m,n))        (one rounding, fp64 -> bf16)
  *
+ * and, with an fp32 addend C[M][N] (oracle_gemm_nt_acc_rows),
+ *
+ *   D(m,n)    = bf16_rne(C(m,n) + acc(m,n))
+ *
  * Sources (page title, section):
  *   - DeepGEMM fp8_gemm.cuh, fp8_gemm_kernel, the math warp-groups: each
  *     128-wide K block is accumulated on its own (the MMA overwrites a fresh
@@ -25,6 +29,9 @@
  *     M-major, [K/128][round_up(M, 4)], one fp32 per row per K block.
  *   - same kernel, the epilogue: the fp32 result is converted to bf16 with
  *     round-to-nearest-even.
+ *   - TCGen05 Copy Instruction (Gluon tutorial), the matmul-accumulate
+ *     example: the fp32 addend C is placed in the accumulator first and the
+ *     product of A and B is accumulated on top of it, so D = A B^T + C.
  *   - the grouped layouts (contiguous: one group index per row; masked: a
  *     per-group valid-row count, rows beyond it untouched) follow the same
  *     file's GemmType::GroupedContiguous / GroupedMasked descriptor shapes.
@@ -257,6 +264,33 @@ void oracle_gemm_grouped_masked_rows(const uint8_t *A, const float *SFA,
             double v = oracle_element_f64(Ag + (long)m * K, Bg + (long)n * K,
                                           SFAg + m, ld,
                                           SFBg + (long)(n / 128) * kb, K);
+            D_rows[(long)i * N + n] = oracle_f64_to_bf16_rne(v);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Plain GEMM with an fp32 addend: D[M][N] = bf16(C[M][N] + A[M][K] * B[N][K]^T
+ * with the scales above).  C is row-major with leading dimension N.  The
+ * addend joins the fp64 sum of the scaled K blocks and the total is rounded
+ * to bf16 once.  Only the listed rows are evaluated; acc_rows (optional)
+ * receives the unrounded values.                                            */
+void oracle_gemm_nt_acc_rows(const uint8_t *A, const float *SFA, const uint8_t *B,
+                             const float *SFB, const float *C, int M, int N, int K,
+                             const int *rows, int nrows, uint16_t *D_rows,
+                             double *acc_rows)
+{
+    long ld = sfa_ld_of(M);
+    int kb = K / 128;
+    for (int i = 0; i < nrows; ++i) {
+        int m = rows[i];
+        for (int n = 0; n < N; ++n) {
+            double v = (double)C[(long)m * N + n] +
+                       oracle_element_f64(A + (long)m * K, B + (long)n * K,
+                                          SFA + m, ld,
+                                          SFB + (long)(n / 128) * kb, K);
+            if (acc_rows)
+                acc_rows[(long)i * N + n] = v;
             D_rows[(long)i * N + n] = oracle_f64_to_bf16_rne(v);
         }
     }

@@ -29,6 +29,11 @@ MUTANTS = {
     "subnormals_as_normals": ("v = ldexp((double)m / 8.0, -6);", "v = ldexp(1.0 + (double)m / 8.0, -7);"),
     "sign_bit_ignored": ("return s ? -v : v;", "return v;"),
     "masked_count_off_by_one": ("if (m < 0 || m >= count || m >= M_max)", "if (m < 0 || m > count || m >= M_max)"),
+    "acc_drops_addend": ("double v = (double)C[(long)m * N + n] +", "double v = 0.0 * (double)C[(long)m * N + n] +"),
+    "acc_addend_transposed": ("C[(long)m * N + n]", "C[(long)n * M + m]"),
+    "acc_addend_subtracted": ("double v = (double)C[(long)m * N + n] +", "double v = -(double)C[(long)m * N + n] +"),
+    "acc_addend_rounded_to_bf16_first": ("double v = (double)C[(long)m * N + n] +",
+                                         "double v = oracle_bf16_to_f64(oracle_f64_to_bf16_rne((double)C[(long)m * N + n])) +"),
     "contiguous_ignores_group": ("const uint8_t *Bg = B + (long)g * N * K;\n        const float *SFBg = SFB + (long)g * nb * kb;",
                                  "const uint8_t *Bg = B;\n        const float *SFBg = SFB;"),
 }
@@ -49,6 +54,9 @@ def _pins():
         ("contig_own_group", lambda lib: pins.test_contiguous_rows_use_their_own_group(lib)),
         ("masked_untouched", lambda lib: pins.test_masked_rows_beyond_count_untouched(lib)),
         ("masked_full", lambda lib: pins.test_masked_full_counts_equal_per_group_dense(lib)),
+        ("acc_zero_addend", lambda lib: pins.test_acc_zero_addend_equals_plain(lib)),
+        ("acc_zero_product", lambda lib: pins.test_acc_zero_product_rounds_the_addend_like_library(lib)),
+        ("acc_exact_integer", lambda lib: pins.test_acc_exact_integer_closed_form(6, 256, 512, lib)),
     ]
 
 

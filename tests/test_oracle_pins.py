@@ -226,6 +226,56 @@ def test_exact_integer_closed_form(M, N, K, lib=None):
     assert np.array_equal(D, torch_bf16_bits(exact.astype(np.float32)))
 
 
+# ---------------------------------------------------------------- the fp32 addend
+
+def test_acc_zero_addend_equals_plain(lib=None):
+    p = wl.make_nt(5, 200, 256, seed=21)
+    D0, acc0 = oracle.gemm_nt(p.A, p.SFA, p.B, p.SFB, p.M, p.N, p.K, want_acc=True, lib=lib)
+    C = np.zeros((p.M, p.N), np.float32)
+    D1, acc1 = oracle.gemm_nt_acc_rows(p.A, p.SFA, p.B, p.SFB, C, p.M, p.N, p.K,
+                                       np.arange(p.M), want_acc=True, lib=lib)
+    assert np.array_equal(D0, D1) and np.array_equal(acc0, acc1)
+
+
+def test_acc_zero_product_rounds_the_addend_like_library(lib=None):
+    """Every A code zero: D is C rounded to bf16, which the library's fp32 ->
+    bf16 cast (round to nearest even) decides.  M != N, so a transposed or
+    wrongly strided C is caught; zeros are left out (0 + -0 is +0)."""
+    M, N, K = 6, 272, 256
+    p = wl.make_nt(M, N, K, seed=22)
+    vals = _random_finite_f32(4 * M * N, 23)
+    vals = vals[vals != 0][:M * N]
+    assert vals.size == M * N
+    C = vals.reshape(M, N)
+    D = oracle.gemm_nt_acc_rows(np.zeros_like(p.A), p.SFA, p.B, p.SFB, C, M, N, K,
+                                np.arange(M), lib=lib)
+    assert np.array_equal(D, torch_bf16_bits(C))
+    # only the listed rows, in the listed order
+    sel = np.array([4, 0], np.int32)
+    Ds = oracle.gemm_nt_acc_rows(np.zeros_like(p.A), p.SFA, p.B, p.SFB, C, M, N, K, sel, lib=lib)
+    assert np.array_equal(Ds, D[sel])
+
+
+@pytest.mark.parametrize("M,N,K", [(6, 256, 512), (5, 384, 1024)])
+def test_acc_exact_integer_closed_form(M, N, K, lib=None):
+    """Small integers with power-of-two scales plus an integer addend: every
+    result is exact in fp32, so D must be the library's cast of the closed
+    form, and the unrounded value the closed form itself."""
+    p = wl.exact_integer_problem(M, N, K, seed=5)
+    z = wl.raw_u64(wl.stream_key(5, 15), 0, M * N)
+    # integers in [-64, 64] plus sixteenths: up to 11 significant bits, more
+    # than bf16 holds, so the addend must enter the sum unrounded
+    C = (((z % np.uint64(129)).astype(np.int64) - 64) +
+         ((z >> np.uint64(32)) % np.uint64(16)).astype(np.int64) / 16.0).astype(np.float32).reshape(M, N)
+    D, acc = oracle.gemm_nt_acc_rows(p.A, p.SFA, p.B, p.SFB, C, M, N, K, np.arange(M),
+                                     want_acc=True, lib=lib)
+    exact = np.array([[float(Fraction(float(C[m, n])) + _exact_value(p, m, n)) for n in range(N)]
+                      for m in range(M)])
+    assert np.array_equal(acc, exact)
+    assert np.array_equal(exact.astype(np.float32).astype(np.float64), exact)
+    assert np.array_equal(D, torch_bf16_bits(exact.astype(np.float32)))
+
+
 # ---------------------------------------------------------------- invariants
 
 def _block_partial(p, m, n, k, g=0):

@@ -21,6 +21,8 @@ Recipe (every workload, seed 0 unless a test says otherwise):
   is 0 gets scale 1 (its codes are all zero whatever the scale).
 * Group sizes (contiguous): uniform integers in [1024, 6144], rounded up to a
   multiple of 128; counts (masked): uniform integers in [0, M_max].
+* The fp32 addend C of the accumulate variant: sqrt(K) * N(0,1), the spread
+  of the product itself (a sum of K products of two N(0,1) values).
 
 Layouts (all C-contiguous):
   A    uint8 [rows][K]          masked: [G][M_max][K]
@@ -28,6 +30,7 @@ Layouts (all C-contiguous):
   B    uint8 [G][N][K]          (G = 1 for the plain GEMM)
   SFB  fp32  [G][ceil(N/128)][K/128]
   D    bf16  [rows][N]          masked: [G][M_max][N]
+  C    fp32  [rows][N]          (accumulate variant only)
 """
 from __future__ import annotations
 
@@ -46,6 +49,7 @@ E4M3_MAX = 448.0
 STREAM_A = 1
 STREAM_B = 2
 STREAM_GROUPS = 3
+STREAM_C = 4
 
 _CHUNK = 1 << 22
 
@@ -198,7 +202,7 @@ def sfa_m_major(scale_rows: np.ndarray, rows: int) -> np.ndarray:
 
 @dataclass
 class Problem:
-    kind: str                       # "nt" | "contiguous" | "masked"
+    kind: str                       # "nt" | "nt_acc" | "contiguous" | "masked"
     M: int                          # nt: M; contiguous: M_total; masked: M_max
     N: int
     K: int
@@ -209,6 +213,7 @@ class Problem:
     SFB: np.ndarray
     m_indices: np.ndarray | None = None   # contiguous, int32 [M_total]
     masked_m: np.ndarray | None = None    # masked, int32 [G]
+    C: np.ndarray | None = None           # nt_acc: fp32 addend [M][N]
     name: str = ""
     meta: dict = field(default_factory=dict)
 
@@ -236,8 +241,8 @@ class Problem:
         return 2 * self.valid_rows() * self.N * self.K
 
     def algorithmic_bytes(self) -> int:
-        """A + SFA + B + SFB + D (+ the group layout), valid rows only; a
-        group's B counts once if the group has any valid row."""
+        """A + SFA + B + SFB + D (+ the group layout, + C), valid rows only;
+        a group's B counts once if the group has any valid row."""
         kb, nb, N, K = self.kb, self.nb, self.N, self.K
         rows = self.valid_rows()
         per_row = K + 4 * kb + 2 * N
@@ -247,7 +252,8 @@ class Problem:
         if self.kind == "contiguous":
             live = len(set(int(g) for g in np.unique(self.m_indices) if 0 <= g < self.G))
             return rows * per_row + live * (N * K + 4 * nb * kb) + 4 * self.M
-        return rows * per_row + N * K + 4 * nb * kb
+        c_bytes = 4 * rows * N if self.C is not None else 0
+        return rows * per_row + N * K + 4 * nb * kb + c_bytes
 
 
 def _quant_A(x: np.ndarray):
@@ -262,6 +268,14 @@ def make_nt(M: int, N: int, K: int, seed: int = 0, name: str = "") -> Problem:
     qb, sb = quantize_blocks_128x128(b)
     return Problem("nt", M, N, K, 1, qa, sfa_m_major(sa, M), qb.reshape(1, N, K),
                    sb.reshape(1, *sb.shape), name=name or f"nt_{M}x{N}x{K}")
+
+
+def make_nt_acc(M: int, N: int, K: int, seed: int = 0, name: str = "") -> Problem:
+    """The plain problem of make_nt plus an fp32 addend C [M][N]."""
+    p = make_nt(M, N, K, seed, name or f"acc_{M}x{N}x{K}")
+    p.kind = "nt_acc"
+    p.C = (normal_f32(seed, STREAM_C, M * N) * np.float32(math.sqrt(K))).reshape(M, N)
+    return p
 
 
 def make_contiguous(group_rows, N: int, K: int, seed: int = 0, name: str = "") -> Problem:
@@ -322,6 +336,8 @@ WORKLOADS = {
         contiguous_group_rows(8, seed=seed), 4096, 7168, seed, "contiguous_g8_n4096_k7168"),
     "masked_g16_m256_n7168_k2048": lambda seed=0: make_masked(
         masked_counts(16, 256, seed=seed), 256, 7168, 2048, seed, "masked_g16_m256_n7168_k2048"),
+    # the accumulate variant (D = bf16(C + A B^T)) on the first dense shape
+    "acc_4096x7168x2048": lambda seed=0: make_nt_acc(4096, 7168, 2048, seed, "acc_4096x7168x2048"),
 }
 
 
