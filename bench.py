@@ -378,6 +378,8 @@ def run_ours(args, dist, ws, rank, local):
                          + " device copies, more than 2 x L2 streamed between two uses of a copy; no flush",
                    "per_kernel_timing": f"{per_case_n} launches of each workload alone, back to back, "
                                         "between one CUDA-event pair on its stream",
+                   **({"addend": "fp32 C [M][N], added once (fp8_gemm_nt_accumulate)"}
+                      if any(c.p.C is not None for c in cases) else {}),
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "flops_per_step": flops_step, "algorithmic_bytes_per_step": bytes_step},
         "shapes": shapes, "roofline": roof,
@@ -440,6 +442,8 @@ def oracle_sample(cases_or_names, budget_s: float, threads: int):
 def _run_rows(oracle, p, rows, threads):
     if p.kind == "nt":
         return oracle.gemm_nt_rows(p.A, p.SFA, p.B, p.SFB, p.M, p.N, p.K, rows, threads=threads)
+    if p.kind == "nt_acc":
+        return oracle.gemm_nt_acc_rows(p.A, p.SFA, p.B, p.SFB, p.C, p.M, p.N, p.K, rows, threads=threads)
     if p.kind == "contiguous":
         return oracle.gemm_grouped_contiguous_rows(p.A, p.SFA, p.B, p.SFB, p.m_indices, p.M, p.N,
                                                    p.K, p.G, rows, threads=threads)

@@ -33,7 +33,7 @@ FP8G_KIND_GROUPED_MASKED = 2
 
 # every symbol the header declares, in declaration order
 EXPORTS = (
-    "fp8_gemm_nt", "fp8_gemm_grouped_contiguous", "fp8_gemm_grouped_masked",
+    "fp8_gemm_nt", "fp8_gemm_nt_accumulate", "fp8_gemm_grouped_contiguous", "fp8_gemm_grouped_masked",
     "fp8_gemm_workspace_size", "fp8_gemm_get_device_error", "fp8_gemm_status_string",
     "fp8_gemm_sfa_ld", "fp8_gemm_set_override", "fp8_gemm_workspace_size_for",
     "fp8_gemm_set_wait_timeout_ns", "fp8_gemm_nt_noalloc", "fp8_gemm_version",
@@ -61,6 +61,8 @@ def library(path: str = LIB_PATH):
         lib = ctypes.CDLL(path)
         vp, sz, i, u64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint64
         lib.fp8_gemm_nt.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp, sz, vp]
+        lib.fp8_gemm_nt_accumulate.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, vp, sz, vp]
+        lib.fp8_gemm_nt_accumulate.restype = i
         lib.fp8_gemm_grouped_contiguous.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, vp, sz, vp]
         lib.fp8_gemm_grouped_masked.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, vp, sz, vp]
         for f in ("fp8_gemm_nt", "fp8_gemm_grouped_contiguous", "fp8_gemm_grouped_masked"):
@@ -118,6 +120,14 @@ def fp8_gemm_nt(A, SFA, B, SFB, D, M, N, K, workspace=None, stream=None) -> int:
     wp, wb = _ws(workspace)
     return library().fp8_gemm_nt(_ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D),
                                  int(M), int(N), int(K), wp, wb, _stream(stream))
+
+
+def fp8_gemm_nt_accumulate(A, SFA, B, SFB, C, D, M, N, K, workspace=None, stream=None) -> int:
+    """D[M][N] (bf16) = C[M][N] (fp32) + the plain product of fp8_gemm_nt.
+    C must not overlap D.  Returns the status code."""
+    wp, wb = _ws(workspace)
+    return library().fp8_gemm_nt_accumulate(_ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(C), _ptr(D),
+                                             int(M), int(N), int(K), wp, wb, _stream(stream))
 
 
 def fp8_gemm_grouped_contiguous(A, SFA, B, SFB, D, m_indices, M_total, N, K, G,

@@ -288,21 +288,12 @@ bool make_maps(LaunchArgs &a, const void *A, const float *SFA, const void *B, co
                        make_pair_map(&a.tmap_b2, B, (uint64_t)b_rows, K, (uint32_t)block_n)));
 }
 
-}  // namespace
-
-// ============================================================================ C ABI
-
-extern "C" {
-
-int fp8_gemm_nt(const void *A, const float *SFA, const void *B, const float *SFB, void *D, int M, int N, int K,
-                void *workspace, size_t workspace_bytes, fp8g_stream_t stream)
+// The plain GEMM, with or without the fp32 addend C (validated by the caller).
+int run_nt(const void *A, const float *SFA, const void *B, const float *SFB, const float *C, void *D, int M, int N,
+           int K, void *workspace, size_t workspace_bytes, fp8g_stream_t stream)
 {
-    int st = check_common(A, SFA, B, SFB, D, M, N, K);
-    if (st != FP8G_OK)
-        return st;
-    if (M == 0 || N == 0)
-        return FP8G_OK;
     DeviceInfo dev;
+    int st;
     if ((st = current_device_info(dev)) != FP8G_OK)
         return st;
     NtChoice c;
@@ -314,6 +305,7 @@ int fp8_gemm_nt(const void *A, const float *SFA, const void *B, const float *SFB
 
     LaunchArgs a;
     fill_common(a.p, M, N, K, 1, SFA, SFB, D, nullptr, c.block_n, dev);
+    a.p.c = C;
     a.p.num_m_blocks = ceil_div(M, 128);
     a.p.group_m = 8;
     a.p.num_tiles = c.tiles;
@@ -328,7 +320,46 @@ int fp8_gemm_nt(const void *A, const float *SFA, const void *B, const float *SFB
         return FP8G_ERR_CUDA;
     a.grid = c.grid;
     a.stream = reinterpret_cast<cudaStream_t>(stream);
-    return to_status(fp8g::launch_nt(c.block_n, c.split_ctas != 0, a));
+    return to_status(C ? fp8g::launch_nt_acc(c.block_n, c.split_ctas != 0, a)
+                       : fp8g::launch_nt(c.block_n, c.split_ctas != 0, a));
+}
+
+}  // namespace
+
+// ============================================================================ C ABI
+
+extern "C" {
+
+int fp8_gemm_nt(const void *A, const float *SFA, const void *B, const float *SFB, void *D, int M, int N, int K,
+                void *workspace, size_t workspace_bytes, fp8g_stream_t stream)
+{
+    int st = check_common(A, SFA, B, SFB, D, M, N, K);
+    if (st != FP8G_OK)
+        return st;
+    if (M == 0 || N == 0)
+        return FP8G_OK;
+    return run_nt(A, SFA, B, SFB, nullptr, D, M, N, K, workspace, workspace_bytes, stream);
+}
+
+int fp8_gemm_nt_accumulate(const void *A, const float *SFA, const void *B, const float *SFB, const float *C,
+                           void *D, int M, int N, int K, void *workspace, size_t workspace_bytes,
+                           fp8g_stream_t stream)
+{
+    int st = check_common(A, SFA, B, SFB, D, M, N, K);
+    if (st != FP8G_OK)
+        return st;
+    if (!C)
+        return FP8G_ERR_INVALID_ARG;
+    if (!aligned(C, 16))
+        return FP8G_ERR_MISALIGNED;
+    if (M == 0 || N == 0)
+        return FP8G_OK;
+    // the kernel reads C through the read-only path while other CTAs write D
+    const uintptr_t c0 = reinterpret_cast<uintptr_t>(C), c1 = c0 + (uintptr_t)M * N * 4;
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(D), d1 = d0 + (uintptr_t)M * N * 2;
+    if (c0 < d1 && d0 < c1)
+        return FP8G_ERR_INVALID_ARG;
+    return run_nt(A, SFA, B, SFB, C, D, M, N, K, workspace, workspace_bytes, stream);
 }
 
 int fp8_gemm_grouped_contiguous(const void *A, const float *SFA, const void *B, const float *SFB, void *D,

@@ -76,7 +76,8 @@ constexpr int kLaunchRegs = 168;
 static_assert(128 * kRegsCtl + 256 * kRegsEpi <= kNumThreads * kLaunchRegs,
               "register reallocation exceeds the launch allocation");
 
-enum Kind : int { kKindNT = 0, kKindContiguous = 1, kKindMasked = 2 };
+// kKindNTAcc: the plain GEMM with an fp32 addend, D = bf16(C + A B^T scaled)
+enum Kind : int { kKindNT = 0, kKindContiguous = 1, kKindMasked = 2, kKindNTAcc = 3 };
 
 template <int BN>
 struct Cfg {
@@ -205,7 +206,7 @@ struct Scheduler {
             w.a_row0 = w.m_blk * kBM;
             w.valid_rows = min(kBM, p.rows - w.a_row0);
             return true;
-        } else if constexpr (KIND == kKindNT) {
+        } else if constexpr (KIND == kKindNT || KIND == kKindNTAcc) {
             if (next_tile >= p.num_tiles)
                 return false;
             const int t = next_tile;
@@ -366,6 +367,90 @@ __device__ __forceinline__ void promote_block(float (&acc)[COLS], uint32_t taddr
             release_tmem(tempty_bar, lane);
         fma_cols<LD>(acc + c * LD, v, s);
     }
+}
+
+// The accumulator's start with an addend (TCGen05 Copy Instruction, the
+// matmul-accumulate example: C is placed in the accumulator before the first
+// product is added).  Only the CTA that stores the tile -- the only one, or a
+// split tile's highest contributor, which holds the last K block -- starts
+// from C; every other contributor starts from zero, so C enters each sum once.
+// The loads are issued before the first MMA completion is awaited.
+template <int BN, int COLS>
+__device__ __forceinline__ void init_from_c(float (&acc)[COLS], const Params &p, const Work &w, int q, int h,
+                                            int lane)
+{
+    const int r = 32 * q + lane;          // row within the tile
+    const int col0 = w.n_blk * BN + h * COLS;
+    const bool live = w.kb1 == p.kb && r < w.valid_rows;
+    // rows are 16-byte aligned (N % 16 == 0, C 16-byte aligned) and col0 is a
+    // multiple of 64, so every float4 below is aligned
+    const float4 *src = reinterpret_cast<const float4 *>(p.c + (size_t)(w.a_row0 + (live ? r : 0)) * p.N + col0);
+#pragma unroll
+    for (int j = 0; j < COLS / 4; ++j) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live && col0 + 4 * j < p.N)
+            v = __ldg(src + j);
+        acc[4 * j] = v.x;
+        acc[4 * j + 1] = v.y;
+        acc[4 * j + 2] = v.z;
+        acc[4 * j + 3] = v.w;
+    }
+}
+
+// With whole-tile staging the addend goes through shared memory instead:
+// each warp's 32 rows x COLS columns of C pass through its staging area --
+// idle between the previous tile's stores and this tile's -- in two rounds of
+// 64 columns, copied by coalesced cp.async (each instruction covers two rows
+// of 256 bytes) and read back one row per thread.  Round 0 is copied three K
+// blocks into the tile; three K blocks before its end round 0 is added and
+// round 1 copied; round 1 is added after the last K block (shorter ranges do
+// both rounds after the loop).  The 16-byte chunk c of row r sits at
+// c ^ (r & 15), so the copies and the row-wise reads both spread over every
+// bank.  (Prefetching C into L2 at the start of the tile, an evict-first L2
+// policy on the copies, other round positions and doing both rounds after the
+// loop were each measured slower or no faster.)
+constexpr int kAddendRoundCols = 64;    // one round: 32 rows x 256 bytes
+
+template <int BN, int COLS>
+__device__ __forceinline__ void copy_c_round(uint8_t *stage, const Params &p, const Work &w, int q, int h, int lane,
+                                             int rows_ok, int rd)
+{
+    const uint32_t s0 = smem_u32(stage);
+    const int c16 = lane & 15;          // the 16-byte chunk this lane copies
+    const int x = w.n_blk * BN + h * COLS + rd * kAddendRoundCols + 4 * c16;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int r = 2 * i + (lane >> 4);
+        const bool live = r < rows_ok && x < p.N;
+        const float *src = live ? p.c + (size_t)(w.a_row0 + 32 * q + r) * p.N + x : p.c;
+        cp_async_16(s0 + r * 256 + ((c16 ^ (r & 15)) << 4), src, live ? 16u : 0u);
+    }
+    cp_async_commit();
+}
+
+template <int COLS>
+__device__ __forceinline__ void add_c_round(float (&acc)[COLS], const uint8_t *stage, int lane, int rd)
+{
+    cp_async_wait_all();
+    __syncwarp();
+    // eight loads in flight before the first of their adds
+    const uint32_t row = smem_u32(stage) + lane * 256;
+#pragma unroll
+    for (int c0 = 0; c0 < 16; c0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            v[c] = ld_shared_f4_nc(row + (((c0 + c) ^ (lane & 15)) << 4));
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float *a = acc + rd * kAddendRoundCols + 4 * (c0 + c);
+            a[0] += v[c].x;
+            a[1] += v[c].y;
+            a[2] += v[c].z;
+            a[3] += v[c].w;
+        }
+    }
+    __syncwarp();                       // read by every lane before the next round lands
 }
 
 // ----------------------------------------------------------------------------
@@ -589,9 +674,24 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         bool ok = true;
         while (ok && sched.next(w)) {
             float acc[COLS];
+            // staged addend (kKindNTAcc, whole-tile staging): the rows this
+            // warp adds C to (none unless this CTA stores the tile), and the
+            // K blocks after which round 0 is copied and then added (with
+            // round 1 copied); short ranges do both rounds after the loop
+            constexpr bool kStagedC = KIND == kKindNTAcc && C::kFullTileStaging;
+            static_assert(!kStagedC || (COLS == 2 * kAddendRoundCols &&
+                                        C::kPanelsPerWarp * C::kPanelBytes >= 32 * kAddendRoundCols * 4),
+                          "addend rounds");
+            const int c_rows = (kStagedC && w.kb1 == p.kb) ? min(max(w.valid_rows - 32 * q, 0), 32) : 0;
+            const bool c_early = w.kb1 - w.kb0 >= 8;
+            const int k_copy0 = w.kb0 + 3, k_add0 = w.kb1 - 3;
+            if constexpr (KIND == kKindNTAcc && !C::kFullTileStaging) {
+                init_from_c<BN, COLS>(acc, p, w, q, h, lane);
+            } else {
 #pragma unroll
-            for (int i = 0; i < COLS; ++i)
-                acc[i] = 0.f;
+                for (int i = 0; i < COLS; ++i)
+                    acc[i] = 0.f;
+            }
 
             for (int k = w.kb0; k < w.kb1; ++k) {
                 // the K block's scales (landed long ago: the producer runs
@@ -633,6 +733,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 promote_block<COLS, 64>(acc, taddr, s, &tempty[acc_ring.i], lane);
                 acc_ring.template next<NACC>();
                 ring.template next<S>();
+                if constexpr (kStagedC) {
+                    if (c_rows > 0 && c_early && k == k_copy0) {
+                        // the previous tile's stores have read the staging area
+                        if (lane == 0)
+                            bulk_wait_group_read<0>();
+                        __syncwarp();
+                        copy_c_round<BN, COLS>(panels, p, w, q, h, lane, c_rows, 0);
+                    }
+                    if (c_rows > 0 && c_early && k == k_add0) {
+                        add_c_round<COLS>(acc, panels, lane, 0);
+                        copy_c_round<BN, COLS>(panels, p, w, q, h, lane, c_rows, 1);
+                    }
+                }
             }
             if (!ok)
                 break;
@@ -710,6 +823,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if (lane == 0)
                     bulk_wait_group_read<0>();
                 __syncwarp();
+                if constexpr (kStagedC) {
+                    if (c_rows > 0) {
+                        if (!c_early) {
+                            copy_c_round<BN, COLS>(panels, p, w, q, h, lane, c_rows, 0);
+                            add_c_round<COLS>(acc, panels, lane, 0);
+                            copy_c_round<BN, COLS>(panels, p, w, q, h, lane, c_rows, 1);
+                        }
+                        add_c_round<COLS>(acc, panels, lane, 1);
+                    }
+                }
             }
             constexpr int PC = C::kPanelCols;
 #pragma unroll
@@ -729,6 +852,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
             }
         }
+        if constexpr (KIND == kKindNTAcc)
+            cp_async_wait_all();        // no addend copy lands after an abort either
         if (lane == 0)
             bulk_wait_group<0>();
         __syncwarp();

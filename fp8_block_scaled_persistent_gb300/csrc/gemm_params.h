@@ -23,6 +23,7 @@ struct Params {
     const float *sfb;
     const int *layout; // contiguous: m_indices; masked: masked_m
     __nv_bfloat16 *d;
+    const float *c;    // NT with an addend: fp32 [rows][N], read-only, not overlapping d
     int num_m_blocks;  // ceil(rows/128) (masked: per group, at most)
     int num_n_blocks;  // ceil(N/BN)
     int group_m;       // rasterisation band height, in m-blocks

@@ -1,5 +1,6 @@
 // launch.h -- host-side launch interface between the C ABI (api.cu) and the
-// kernel instantiations (gemm_nt.cu, gemm_contiguous.cu, gemm_masked.cu).
+// kernel instantiations (gemm_nt.cu, gemm_nt_acc.cu, gemm_contiguous.cu,
+// gemm_masked.cu).
 #pragma once
 
 #include <cuda.h>
@@ -27,6 +28,7 @@ int smem_bytes_for(int block_n);
 int panel_cols_for(int block_n);
 
 cudaError_t launch_nt(int block_n, bool split, const LaunchArgs &a);
+cudaError_t launch_nt_acc(int block_n, bool split, const LaunchArgs &a);   // a.p.c set
 cudaError_t launch_contiguous(int block_n, const LaunchArgs &a);
 cudaError_t launch_masked(int block_n, const LaunchArgs &a);
 

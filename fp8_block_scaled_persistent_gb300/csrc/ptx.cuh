@@ -446,6 +446,30 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+// A 16-byte shared-memory load without a compiler memory barrier: volatile
+// asm keeps it after earlier volatile asm (a wait) yet lets several loads
+// issue before their first use.
+__device__ __forceinline__ float4 ld_shared_f4_nc(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// 16 bytes global -> shared through L2 (cp.async.cg); src_bytes (0 or 16) of
+// them are read, the rest of the 16 are zero-filled.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ float ld_nc_f32(const float *p)
 {
     float v;

@@ -1,7 +1,7 @@
 /*
  * fp8gemm.h -- C ABI of the GB300 (sm_103a) FP8 block-scaled GEMM library.
  *
- * Operation (all three entry points):
+ * Operation (every GEMM entry point; fp8_gemm_nt_accumulate adds C first):
  *
  *   D[m][n] = bf16( sum_{k < K/128} SFA[k][m] * SFB[n/128][k] *
  *                   sum_{t < 128} A[m][128k+t] * B[n][128k+t] )
@@ -89,6 +89,26 @@ int fp8_gemm_nt(const void *A, const float *SFA, const void *B, const float *SFB
                 void *workspace, size_t workspace_bytes, fp8g_stream_t stream);
 
 /*
+ * Plain GEMM with an fp32 addend:
+ *   D[m][n] = bf16( C[m][n] + sum_k SFA[k][m] * SFB[n/128][k] * S_k(m, n) )
+ * with S_k the 128-wide K block's product of A and B as above.  C is DEVICE
+ * fp32 [M][N] (row-major, leading dimension N), 16-byte aligned, read only,
+ * and must not overlap D; D keeps fp8_gemm_nt's bf16 layout.  The addend
+ * starts the fp32 accumulator of the block that stores the tile, so it is
+ * added exactly once; the result is rounded to bf16 once.
+ * Source: TCGen05 Copy Instruction (Triton Gluon tutorial), the matmul-
+ * accumulate example (C is placed in the accumulator, then the product of A
+ * and B is accumulated on top of it).
+ * Everything else -- requirements, workspace (size from fp8_gemm_workspace_size
+ * with kind FP8G_KIND_NT), schedules, errors -- is fp8_gemm_nt's.  C == NULL or
+ * C overlapping D returns FP8G_ERR_INVALID_ARG, a C not 16-byte aligned
+ * FP8G_ERR_MISALIGNED; M == 0 or N == 0 is a no-op.
+ */
+int fp8_gemm_nt_accumulate(const void *A, const float *SFA, const void *B, const float *SFB,
+                           const float *C, void *D, int M, int N, int K,
+                           void *workspace, size_t workspace_bytes, fp8g_stream_t stream);
+
+/*
  * Grouped GEMM, contiguous layout (MoE experts): rows of A are concatenated
  * over groups; m_indices[r] (device int32 [M_total]) names the group of row
  * r, and row r is multiplied by B[m_indices[r]].  Every 128-row block must
@@ -122,7 +142,8 @@ int fp8_gemm_grouped_masked(const void *A, const float *SFA, const void *B,
 
 /*
  * Bytes of workspace the given problem can use (0 if it never splits K).
- * kind is an fp8g_kind; for NT pass G = 1; M is M, M_total or M_max.
+ * kind is an fp8g_kind (FP8G_KIND_NT also for fp8_gemm_nt_accumulate); for NT
+ * pass G = 1; M is M, M_total or M_max.
  * Pure host function: needs no GPU.  Assumes the current device's SM count
  * if a device is present, else 152.
  */

@@ -19,6 +19,8 @@ def dev_tensors(p, device="cuda"):
         t["layout"] = torch.from_numpy(np.ascontiguousarray(p.m_indices, dtype=np.int32)).to(device)
     if p.masked_m is not None:
         t["layout"] = torch.from_numpy(np.ascontiguousarray(p.masked_m, dtype=np.int32)).to(device)
+    if p.C is not None:
+        t["C"] = torch.from_numpy(np.ascontiguousarray(p.C, dtype=np.float32)).to(device)
     return t
 
 
@@ -34,6 +36,9 @@ def call(p, t, D, workspace=None, stream=None, layout=None) -> int:
     if p.kind == "nt":
         return fg.fp8_gemm_nt(t["A"], t["SFA"], t["B"], t["SFB"], D, p.M, p.N, p.K,
                               workspace=workspace, stream=stream)
+    if p.kind == "nt_acc":
+        return fg.fp8_gemm_nt_accumulate(t["A"], t["SFA"], t["B"], t["SFB"], t["C"], D, p.M, p.N, p.K,
+                                         workspace=workspace, stream=stream)
     lay = t["layout"] if layout is None else layout
     if p.kind == "contiguous":
         return fg.fp8_gemm_grouped_contiguous(t["A"], t["SFA"], t["B"], t["SFB"], D, lay,
@@ -52,7 +57,7 @@ def workspace_for(p, device="cuda"):
     """A zero-filled workspace of the size the library asks for (None if 0)."""
     import torch
     import fp8_block_scaled_persistent_gb300 as fg
-    kind = {"nt": 0, "contiguous": 1, "masked": 2}[p.kind]
+    kind = {"nt": 0, "nt_acc": 0, "contiguous": 1, "masked": 2}[p.kind]
     n = fg.fp8_gemm_workspace_size(kind, p.M, p.N, p.K, p.G)
     if n == 0:
         return None

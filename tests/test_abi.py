@@ -66,6 +66,19 @@ def test_nt_validation(lib, args, status):
     assert fg.fp8_gemm_nt(*args, workspace=None, stream=0) == status
 
 
+def test_nt_accumulate_validation(lib):
+    a = fg.fp8_gemm_nt_accumulate
+    M, N, K = 128, 256, 512
+    assert a(FAKE, FAKE, FAKE, FAKE, 0, FAKE, M, N, K, stream=0) == fg.FP8G_ERR_INVALID_ARG      # no C
+    assert a(FAKE, FAKE, FAKE, FAKE, FAKE + 4, FAKE, M, N, K, stream=0) == fg.FP8G_ERR_MISALIGNED
+    assert a(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, M, N, 500, stream=0) == fg.FP8G_ERR_UNSUPPORTED
+    c = FAKE + (1 << 24)
+    # C [M][N] fp32 and D [M][N] bf16 overlapping, either way round
+    assert a(FAKE, FAKE, FAKE, FAKE, c, c + 4 * M * N - 16, M, N, K, stream=0) == fg.FP8G_ERR_INVALID_ARG
+    assert a(FAKE, FAKE, FAKE, FAKE, c, c - 2 * M * N + 16, M, N, K, stream=0) == fg.FP8G_ERR_INVALID_ARG
+    assert a(FAKE, FAKE, FAKE, FAKE, c, c, 0, N, K, stream=0) == fg.FP8G_OK        # empty: no-op
+
+
 def test_grouped_validation(lib):
     c = fg.fp8_gemm_grouped_contiguous
     assert c(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 256, 256, 512, 2, stream=0) == fg.FP8G_ERR_INVALID_ARG
