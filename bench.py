@@ -530,6 +530,12 @@ def main(argv=None):
             v, dt, sample = oracle_sample(cases, args.cpu_budget, threads)
             out["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                    "sample": sample, "seconds": dt}
+            # the same oracle on one core, over a smaller row sample; the rate
+            # is what the whole workload would take at that pace (extrapolated)
+            v1, dt1, sample1 = oracle_sample(cases, max(1.0, args.cpu_budget / 5), 1)
+            out["cpu_baseline"]["single_core"] = {
+                "value": v1, "unit": "TFLOP/s", "cores": 1, "sample": sample1, "seconds": dt1,
+                "full_step_seconds_extrapolated": sum(c.flops for c in cases) / (v1 * 1e12)}
         print(json.dumps(out), flush=True)
     if dist is not None:
         dist.destroy_process_group()
