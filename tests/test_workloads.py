@@ -65,3 +65,19 @@ def test_problem_accounting():
     p = wl.make_nt(128, 256, 512)
     assert p.flops() == 2 * 128 * 256 * 512
     assert p.algorithmic_bytes() == 264_224
+
+
+def test_addend_recipe():
+    """The accumulate variant's C: fp32 [M][N], sqrt(K) * N(0,1) from its own
+    stream, the plain problem's A and B unchanged, C counted in the bytes."""
+    M, N, K = 130, 256, 1024
+    p = wl.make_nt_acc(M, N, K, seed=3)
+    q = wl.make_nt(M, N, K, seed=3)
+    assert p.kind == "nt_acc" and p.C.shape == (M, N) and p.C.dtype == np.float32
+    assert np.array_equal(p.A, q.A) and np.array_equal(p.B, q.B)
+    assert np.array_equal(p.C, wl.make_nt_acc(M, N, K, seed=3).C)
+    want = (wl.normal_f32(3, wl.STREAM_C, M * N) * np.float32(np.sqrt(K))).reshape(M, N)
+    assert np.array_equal(p.C, want)
+    assert 0.9 * np.sqrt(K) < p.C.std() < 1.1 * np.sqrt(K)
+    assert p.flops() == q.flops()
+    assert p.algorithmic_bytes() == q.algorithmic_bytes() + 4 * M * N
