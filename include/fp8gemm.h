@@ -93,9 +93,10 @@ int fp8_gemm_nt(const void *A, const float *SFA, const void *B, const float *SFB
  *   D[m][n] = bf16( C[m][n] + sum_k SFA[k][m] * SFB[n/128][k] * S_k(m, n) )
  * with S_k the 128-wide K block's product of A and B as above.  C is DEVICE
  * fp32 [M][N] (row-major, leading dimension N), 16-byte aligned, read only,
- * and must not overlap D; D keeps fp8_gemm_nt's bf16 layout.  The addend
- * starts the fp32 accumulator of the block that stores the tile, so it is
- * added exactly once; the result is rounded to bf16 once.
+ * and must not overlap D; D keeps fp8_gemm_nt's bf16 layout.  Only the
+ * thread block that stores a tile adds C into its fp32 accumulator, so C is
+ * added exactly once (also when K is split across blocks); the result is
+ * rounded to bf16 once.
  * Source: TCGen05 Copy Instruction (Triton Gluon tutorial), the matmul-
  * accumulate example (C is placed in the accumulator, then the product of A
  * and B is accumulated on top of it).
