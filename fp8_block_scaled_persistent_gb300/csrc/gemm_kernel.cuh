@@ -399,25 +399,25 @@ __device__ __forceinline__ void init_from_c(float (&acc)[COLS], const Params &p,
 
 // With whole-tile staging the addend goes through shared memory instead:
 // each warp's 32 rows x COLS columns of C pass through its staging area --
-// idle between the previous tile's stores and this tile's -- in two rounds of
-// 64 columns, copied by coalesced cp.async (each instruction covers two rows
-// of 256 bytes) and read back one row per thread.  Round 0 is copied three K
-// blocks into the tile; three K blocks before its end round 0 is added and
-// round 1 copied; round 1 is added after the last K block (shorter ranges do
-// both rounds after the loop).  The 16-byte chunk c of row r sits at
+// idle between the previous tile's stores and this tile's -- one half (64
+// columns) at a time, copied by coalesced cp.async (each instruction covers
+// two rows of 256 bytes) and read back one row per thread.  Half 0 is copied
+// three K blocks into the tile; three K blocks before its end half 0 is added
+// and half 1 copied; half 1 is added after the last K block (shorter ranges
+// do both halves after the loop).  The 16-byte chunk c of row r sits at
 // c ^ (r & 15), so the copies and the row-wise reads both spread over every
 // bank.  (Prefetching C into L2 at the start of the tile, an evict-first L2
-// policy on the copies, other round positions and doing both rounds after the
+// policy on the copies, other copy positions and doing both halves after the
 // loop were each measured slower or no faster.)
-constexpr int kAddendRoundCols = 64;    // one round: 32 rows x 256 bytes
+constexpr int kAddendHalfCols = 64;     // one half: 32 rows x 256 bytes
 
 template <int BN, int COLS>
-__device__ __forceinline__ void copy_c_round(uint8_t *stage, const Params &p, const Work &w, int q, int h, int lane,
+__device__ __forceinline__ void copy_c_half(uint8_t *stage, const Params &p, const Work &w, int q, int h, int lane,
                                              int rows_ok, int rd)
 {
     const uint32_t s0 = smem_u32(stage);
     const int c16 = lane & 15;          // the 16-byte chunk this lane copies
-    const int x = w.n_blk * BN + h * COLS + rd * kAddendRoundCols + 4 * c16;
+    const int x = w.n_blk * BN + h * COLS + rd * kAddendHalfCols + 4 * c16;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const int r = 2 * i + (lane >> 4);
@@ -429,7 +429,7 @@ __device__ __forceinline__ void copy_c_round(uint8_t *stage, const Params &p, co
 }
 
 template <int COLS>
-__device__ __forceinline__ void add_c_round(float (&acc)[COLS], const uint8_t *stage, int lane, int rd)
+__device__ __forceinline__ void add_c_half(float (&acc)[COLS], const uint8_t *stage, int lane, int rd)
 {
     cp_async_wait_all();
     __syncwarp();
@@ -443,14 +443,14 @@ __device__ __forceinline__ void add_c_round(float (&acc)[COLS], const uint8_t *s
             v[c] = ld_shared_f4_nc(row + (((c0 + c) ^ (lane & 15)) << 4));
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            float *a = acc + rd * kAddendRoundCols + 4 * (c0 + c);
+            float *a = acc + rd * kAddendHalfCols + 4 * (c0 + c);
             a[0] += v[c].x;
             a[1] += v[c].y;
             a[2] += v[c].z;
             a[3] += v[c].w;
         }
     }
-    __syncwarp();                       // read by every lane before the next round lands
+    __syncwarp();                       // read by every lane before the next half lands
 }
 
 // ----------------------------------------------------------------------------
@@ -676,12 +676,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             float acc[COLS];
             // staged addend (kKindNTAcc, whole-tile staging): the rows this
             // warp adds C to (none unless this CTA stores the tile), and the
-            // K blocks after which round 0 is copied and then added (with
-            // round 1 copied); short ranges do both rounds after the loop
+            // K blocks after which half 0 is copied and then added (with
+            // half 1 copied); short ranges do both halves after the loop
             constexpr bool kStagedC = KIND == kKindNTAcc && C::kFullTileStaging;
-            static_assert(!kStagedC || (COLS == 2 * kAddendRoundCols &&
-                                        C::kPanelsPerWarp * C::kPanelBytes >= 32 * kAddendRoundCols * 4),
-                          "addend rounds");
+            static_assert(!kStagedC || (COLS == 2 * kAddendHalfCols &&
+                                        C::kPanelsPerWarp * C::kPanelBytes >= 32 * kAddendHalfCols * 4),
+                          "addend halves");
             const int c_rows = (kStagedC && w.kb1 == p.kb) ? min(max(w.valid_rows - 32 * q, 0), 32) : 0;
             const bool c_early = w.kb1 - w.kb0 >= 8;
             const int k_copy0 = w.kb0 + 3, k_add0 = w.kb1 - 3;
@@ -739,11 +739,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         if (lane == 0)
                             bulk_wait_group_read<0>();
                         __syncwarp();
-                        copy_c_round<BN, COLS>(panels, p, w, q, h, lane, c_rows, 0);
+                        copy_c_half<BN, COLS>(panels, p, w, q, h, lane, c_rows, 0);
                     }
                     if (c_rows > 0 && c_early && k == k_add0) {
-                        add_c_round<COLS>(acc, panels, lane, 0);
-                        copy_c_round<BN, COLS>(panels, p, w, q, h, lane, c_rows, 1);
+                        add_c_half<COLS>(acc, panels, lane, 0);
+                        copy_c_half<BN, COLS>(panels, p, w, q, h, lane, c_rows, 1);
                     }
                 }
             }
@@ -826,11 +826,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if constexpr (kStagedC) {
                     if (c_rows > 0) {
                         if (!c_early) {
-                            copy_c_round<BN, COLS>(panels, p, w, q, h, lane, c_rows, 0);
-                            add_c_round<COLS>(acc, panels, lane, 0);
-                            copy_c_round<BN, COLS>(panels, p, w, q, h, lane, c_rows, 1);
+                            copy_c_half<BN, COLS>(panels, p, w, q, h, lane, c_rows, 0);
+                            add_c_half<COLS>(acc, panels, lane, 0);
+                            copy_c_half<BN, COLS>(panels, p, w, q, h, lane, c_rows, 1);
                         }
-                        add_c_round<COLS>(acc, panels, lane, 1);
+                        add_c_half<COLS>(acc, panels, lane, 1);
                     }
                 }
             }
