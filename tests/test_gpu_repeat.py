@@ -1,0 +1,40 @@
+"""Repeated launches give the same bits.
+
+The paths where a missing fence or barrier would show up only now and then:
+the split-K reduction across CTAs (published partials, counters), the staged
+addend (copies into the staging area the previous tile's stores read) and
+the masked layout's untouched rows.  Each workload runs many times back to
+back on one stream with the inputs resident; every output must be bit-identical
+to the first, and the split-K counters must be back at zero.
+"""
+import numpy as np
+import pytest
+
+import workloads as wl
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name,reps", [
+    ("smallm_128x7168x16384", 16), ("smallm_64x7168x16384", 16),
+    ("acc_4096x7168x2048", 8), ("masked_g16_m256_n7168_k2048", 8)])
+def test_repeated_launches_bit_identical(name, reps):
+    import torch
+    import fp8_block_scaled_persistent_gb300 as fg
+    p = wl.make(name)
+    t = gu.dev_tensors(p)
+    ws = gu.workspace_for(p)
+    outs = []
+    for _ in range(reps):
+        D = gu.new_d(p)
+        assert gu.call(p, t, D, workspace=ws) == fg.FP8G_OK
+        outs.append(D)
+    assert fg.fp8_gemm_get_device_error() == fg.FP8G_OK
+    first = gu.bits(outs[0])
+    for i, D in enumerate(outs[1:], 1):
+        assert np.array_equal(gu.bits(D), first), f"{name}: launch {i} differs from launch 0"
+    if ws is not None:
+        # the counters (8 per 128-column tile) lead the workspace
+        tiles = ((p.M + 127) // 128) * ((p.N + 127) // 128)
+        assert int(ws[: tiles * 8 * 4].view(torch.int32).abs().sum()) == 0
