@@ -350,18 +350,23 @@ __device__ __forceinline__ void release_tmem(uint64_t *bar, int lane)
 }
 
 // acc[0 .. COLS) += s * (this thread's row of the K block's partial in TMEM,
-// columns taddr.col .. +COLS), LD columns per tcgen05.ld.  The buffer is
-// handed back to the MMA issuer as soon as its last load landed.
+// columns taddr.col .. +COLS), LD columns per tcgen05.ld, with s = *pa * *pb
+// (the K block's A and B scales in shared memory), read while the first TMEM
+// load is in flight.  The buffer is handed back to the MMA issuer as soon as
+// its last load landed.
 template <int COLS, int LD>
-__device__ __forceinline__ void promote_block(float (&acc)[COLS], uint32_t taddr, float s, uint64_t *tempty_bar,
-                                              int lane)
+__device__ __forceinline__ void promote_block(float (&acc)[COLS], uint32_t taddr, const float *pa, const float *pb,
+                                              uint64_t *tempty_bar, int lane)
 {
     constexpr int NCH = COLS / LD;
     static_assert(COLS % LD == 0, "column split");
+    float s = 0.f;
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
         uint32_t v[LD];
         tmem_ld(taddr + c * LD, v);
+        if (c == 0)
+            s = *pa * *pb;
         tmem_wait_ld(v);
         if (c + 1 == NCH)
             release_tmem(tempty_bar, lane);
@@ -713,26 +718,28 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 __syncwarp();           // orders lane 0's barrier waits before every lane's reads
                 tc_fence_after_sync();
+                // the scales are read inside promote_block, after the first
+                // TMEM load is issued; the B part starts at the aligned group
+                // of 4 that holds the chunk's first B scale, and the flat SFB
+                // index picks the element
                 const uint8_t *slot = sm_scales + sring.i * C::kSlotBytes;
-                const float sa = reinterpret_cast<const float *>(slot)[kc * kBM + row_in_tile];
-                // the B part starts at the aligned group of 4 that holds the
-                // chunk's first B scale: the flat SFB index picks the element
+                const float *pa = reinterpret_cast<const float *>(slot) + kc * kBM + row_in_tile;
                 const int sfb_idx0 = (w.g * p.nb + (w.n_blk * BN) / 128 + sfb_row) * p.kb + k0;
-                const float sb = reinterpret_cast<const float *>(slot + C::kSlotSfaBytes +
-                                                                 C::kSlotSfbStride * sfb_row)[(sfb_idx0 & 3) + kc];
-                const float s = sa * sb;
+                const float *pb = reinterpret_cast<const float *>(slot + C::kSlotSfaBytes +
+                                                                  C::kSlotSfbStride * sfb_row) + (sfb_idx0 & 3) + kc;
+
+                const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + acc_ring.i * BN + h * COLS;
+                promote_block<COLS, 64>(acc, taddr, pa, pb, &tempty[acc_ring.i], lane);
+                acc_ring.template next<NACC>();
+                ring.template next<S>();
                 if (kc == kScaleChunk - 1 || k + 1 == w.kb1) {
                     // last K block of the chunk: the slot may be refilled
+                    // (released after the TMEM buffer, off its critical path)
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(&sempty[sring.i]);
                     sring.template next<SR>();
                 }
-
-                const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + acc_ring.i * BN + h * COLS;
-                promote_block<COLS, 64>(acc, taddr, s, &tempty[acc_ring.i], lane);
-                acc_ring.template next<NACC>();
-                ring.template next<S>();
                 if constexpr (kStagedC) {
                     if (c_rows > 0 && c_early && k == k_copy0) {
                         // the previous tile's stores have read the staging area
