@@ -44,6 +44,7 @@ def _pins():
     return [
         ("decode_vs_library", lambda lib: pins.test_e4m3_decode_exhaustive_matches_library(lib)),
         ("special_values", lambda lib: pins.test_e4m3_special_values_golden(lib)),
+        ("e4m3_round_trips", lambda lib: pins.test_e4m3_quantise_dequantise_round_trips(lib)),
         ("bf16_vs_library", lambda lib: pins.test_bf16_rne_matches_library_on_f32_values(lib)),
         ("bf16_fp64_cases", lambda lib: pins.test_bf16_rne_fp64_only_cases(lib)),
         ("hand_worked", lambda lib: [pins.test_hand_worked_elements(c, lib) for c in cases]),

@@ -136,6 +136,29 @@ def test_bf16_rne_fp64_only_cases(lib=None):
     assert f(float("nan")) == 0x7FC0
 
 
+def test_e4m3_quantise_dequantise_round_trips(lib=None):
+    """The input generator's encoder against the oracle's decoder:
+    encode(decode(q)) == q for every non-NaN code, and for values inside the
+    finite range decode(encode(x)) is within half an E4M3 ulp of x, ties
+    going to the code with an even mantissa."""
+    codes = [q for q in range(256) if q not in (0x7F, 0xFF)]
+    dec = np.array([oracle.e4m3_to_f64(q, lib=lib) for q in codes])
+    assert np.array_equal(wl.e4m3_encode(dec.astype(np.float32)), np.array(codes, np.uint8))
+    x = np.concatenate([wl.normal_f32(0, 60, 20_000) * 60, wl.normal_f32(0, 61, 20_000) * 0.02,
+                        # exact midpoints between neighbouring codes (ties)
+                        ((dec[1:120] + dec[2:121]) / 2).astype(np.float32)]).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    q = wl.e4m3_encode(x)
+    back = np.array([oracle.e4m3_to_f64(int(c), lib=lib) for c in q])
+    a = np.abs(x.astype(np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -6)))
+    ulp = 2.0 ** (e - 3)                 # 3 mantissa bits; subnormals share 2^-9
+    err = np.abs(back - x)
+    assert (err <= ulp / 2).all()
+    tie = err == ulp / 2
+    assert tie.any() and ((q[tie] & 1) == 0).all()
+
+
 def test_bf16_decode_roundtrip(lib=None):
     for h in range(0, 0x10000, 37):
         v = oracle.bf16_to_f64(h, lib=lib)
