@@ -45,3 +45,19 @@ def test_other_ranks_exit_quietly():
 def test_warmup_below_three_is_refused():
     r = _run({}, "--steps", "2", "--warmup", "2")
     assert r.returncode != 0
+
+
+def test_traffic_lookup(tmp_path, monkeypatch):
+    """roofline.traffic comes from profiles/traffic.txt: bytes for a listed
+    workload, None for one that is not listed or marked none."""
+    sys.path.insert(0, ROOT)
+    import bench
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.txt").write_text(
+        "# comment line\nworkload_a 12345\nworkload_b none\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_traffic("workload_a") == 12345
+    assert bench.load_traffic("workload_b") is None
+    assert bench.load_traffic("workload_c") is None
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path / "missing"))
+    assert bench.load_traffic("workload_a") is None

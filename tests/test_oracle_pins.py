@@ -412,6 +412,16 @@ def test_row_driver_threads_bitwise(lib=None):
     assert np.array_equal(Ds, D1[sel])
 
 
+def test_acc_row_driver_threads_bitwise(lib=None):
+    p = wl.make_nt_acc(40, 272, 384, seed=15)
+    rows = np.arange(p.M)
+    one, acc1 = oracle.gemm_nt_acc_rows(p.A, p.SFA, p.B, p.SFB, p.C, p.M, p.N, p.K, rows,
+                                        threads=1, want_acc=True, lib=lib)
+    four, acc4 = oracle.gemm_nt_acc_rows(p.A, p.SFA, p.B, p.SFB, p.C, p.M, p.N, p.K, rows,
+                                         threads=4, want_acc=True, lib=lib)
+    assert np.array_equal(one, four) and np.array_equal(acc1, acc4)
+
+
 def test_element_matches_full_product(lib=None):
     p = wl.make_nt(3, 260, 384, seed=14)
     _, acc = oracle.gemm_nt(p.A, p.SFA, p.B, p.SFB, p.M, p.N, p.K, want_acc=True, lib=lib)
