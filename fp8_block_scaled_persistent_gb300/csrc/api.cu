@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -31,6 +32,33 @@ __device__ int g_error_word;              // sticky device-side error bits, per 
 
 std::atomic<int> g_override_bn{0};
 std::atomic<int> g_override_split{0};
+
+// FP8G_FORCE_CONFIG="block_n[,split_ctas]" sets the tuning overrides when the
+// library loads (the values fp8_gemm_set_override accepts); a malformed value
+// is ignored, leaving the automatic choice.
+struct EnvOverride {
+    EnvOverride()
+    {
+        const char *v = std::getenv("FP8G_FORCE_CONFIG");
+        if (!v || !*v)
+            return;
+        char *end = nullptr;
+        const long bn = std::strtol(v, &end, 10);
+        long split = 0;
+        if (end == v || (bn != 0 && bn != 128 && bn != 256))
+            return;
+        if (*end == ',') {
+            const char *s = end + 1;
+            split = std::strtol(s, &end, 10);
+            if (end == s || split < -1000000 || split > 1000000)
+                return;
+        }
+        if (*end != '\0')
+            return;
+        g_override_bn.store((int)bn);
+        g_override_split.store((int)split);
+    }
+} g_env_override;
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 
 // ------------------------------------------------------------ device facts

@@ -169,7 +169,10 @@ int fp8_gemm_sfa_ld(int M);
  *   split_ctas  : > 0 forces the split-K schedule over that many CTAs (with
  *                 128-column tiles unless block_n says 256; needs a workspace
  *                 of fp8_gemm_workspace_size_for bytes), < 0 forbids splitting.
- * Returns FP8G_ERR_INVALID_ARG for values outside those sets.
+ * Returns FP8G_ERR_INVALID_ARG for values outside those sets.  The
+ * environment variable FP8G_FORCE_CONFIG="block_n[,split_ctas]", read when
+ * the library loads, sets the same values (a malformed value is ignored);
+ * this call replaces them.
  */
 int fp8_gemm_set_override(int block_n, int split_ctas);
 

@@ -110,3 +110,33 @@ def test_workspace_sizes_host_only(lib):
     n = fg.fp8_gemm_workspace_size_for(128, 256, 1024, 128, 10)
     assert n == 256 + 2 * 10 * 128 * 128 * 4
     assert fg.fp8_gemm_version() == 10000
+
+
+@pytest.mark.parametrize("value,dense,smallm", [
+    ("", 0, "auto"),
+    ("128,8", "forced", "forced_small"),
+    ("256,-1", 0, 0),
+    ("bogus", 0, "auto"),
+    ("100,4", 0, "auto"),
+    ("128,8x", 0, "auto"),
+])
+def test_force_config_environment(lib, value, dense, smallm):
+    """FP8G_FORCE_CONFIG sets the tuning overrides when the library loads;
+    malformed values leave the automatic choice.  Observed through the
+    workspace sizes the schedule choice implies (no GPU needed)."""
+    import subprocess
+    import sys
+    code = ("import fp8_block_scaled_persistent_gb300 as fg; "
+            "print(fg.fp8_gemm_workspace_size(0, 4096, 7168, 2048, 1), "
+            "fg.fp8_gemm_workspace_size(0, 128, 7168, 16384, 1))")
+    env = dict(os.environ, FP8G_FORCE_CONFIG=value, CUDA_VISIBLE_DEVICES="")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                         cwd=ROOT, check=True).stdout.split()
+    got_dense, got_small = int(out[0]), int(out[1])
+    want = {
+        0: 0,
+        "auto": fg.fp8_gemm_workspace_size(0, 128, 7168, 16384, 1),
+        "forced": fg.fp8_gemm_workspace_size_for(4096, 7168, 2048, 128, 8),
+        "forced_small": fg.fp8_gemm_workspace_size_for(128, 7168, 16384, 128, 8),
+    }
+    assert got_dense == want[dense] and got_small == want[smallm]
