@@ -412,10 +412,11 @@ def load_traffic(name):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def oracle_sample(cases_or_names, budget_s: float, threads: int):
+def oracle_sample(cases_or_names, budget_s: float, threads: int, refs=None):
     """Times the CPU oracle on a bounded sample: for each workload, rows of the
     output (all columns), as many rows as fit the time budget.  Returns
-    (TFLOP/s, seconds, description)."""
+    (TFLOP/s, seconds, description); appends (problem, rows, oracle rows) to
+    `refs` when given."""
     import oracle
     probs = []
     for c in cases_or_names:
@@ -432,7 +433,9 @@ def oracle_sample(cases_or_names, budget_s: float, threads: int):
     desc = []
     for p in probs:
         r = np.linspace(0, p.M - 1, num=min(rows, p.M)).astype(np.int32)
-        _run_rows(oracle, p, r, threads)
+        ref = _run_rows(oracle, p, r, threads)
+        if refs is not None:
+            refs.append((p, r, ref))
         macs += len(r) * p.N * p.K
         desc.append(f"{len(r)} rows x {p.N} cols of {p.name}")
     dt = time.time() - t0
@@ -451,6 +454,31 @@ def _run_rows(oracle, p, rows, threads):
     rows = rows[rows < int(p.masked_m[g])]
     return oracle.gemm_grouped_masked_rows(p.A, p.SFA, p.B, p.SFB, p.masked_m, p.G, p.M, p.N, p.K,
                                            g, rows, threads=threads)
+
+
+def parity_of(cases, refs):
+    """The GPU output the timed launches left in each workload's D against
+    the oracle rows of the CPU sample, with the method's tolerance."""
+    from tests import gpu_util as gu
+    from tests.tolerance import check
+    out = {"rows": 0, "elements": 0, "max_err_over_bound": 0.0, "global_diff": 0.0, "ok": True}
+    for c, (p, r, ref) in zip(cases, refs):
+        d = gu.bits(c.D)
+        if p.kind == "masked":
+            g = int(np.argmax(p.masked_m))
+            r = r[r < int(p.masked_m[g])]
+            d = d[g]
+        try:
+            st = check(d[r], ref, p.name)
+        except AssertionError as e:
+            out["ok"] = False
+            out.setdefault("failures", []).append(str(e))
+            continue
+        out["rows"] += len(r)
+        out["elements"] += st["elements"]
+        out["max_err_over_bound"] = max(out["max_err_over_bound"], st["max_err_over_bound"])
+        out["global_diff"] = max(out["global_diff"], st["global_diff"])
+    return out
 
 
 def run_reference(args, rank):
@@ -527,9 +555,12 @@ def main(argv=None):
         if not args.no_cpu_baseline:
             import oracle
             threads = oracle.default_threads()
-            v, dt, sample = oracle_sample(cases, args.cpu_budget, threads)
+            refs = []
+            v, dt, sample = oracle_sample(cases, args.cpu_budget, threads, refs)
             out["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                    "sample": sample, "seconds": dt}
+            # the measured output itself, on the rows the oracle just computed
+            out["parity"] = parity_of(cases, refs)
             # the same oracle on one core, over a smaller row sample; the rate
             # is what the whole workload would take at that pace (extrapolated)
             v1, dt1, sample1 = oracle_sample(cases, max(1.0, args.cpu_budget / 5), 1)
