@@ -64,6 +64,10 @@ def _bind(lib):
     lib.oracle_gemm_nt_acc_rows.restype = None
     lib.oracle_gemm_nt_acc_rows.argtypes = [u8p, f32p, u8p, f32p, f32p, I, I, I,
                                             i32p, I, u16p, f64p]
+    lib.oracle_ue8m0_to_f64.restype = ctypes.c_double
+    lib.oracle_ue8m0_to_f64.argtypes = [ctypes.c_uint8]
+    lib.oracle_gemm_nt_ue8m0_rows.restype = None
+    lib.oracle_gemm_nt_ue8m0_rows.argtypes = [u8p, u8p, u8p, u8p, I, I, I, i32p, I, u16p, f64p]
     lib.oracle_gemm_grouped_contiguous_rows.restype = None
     lib.oracle_gemm_grouped_contiguous_rows.argtypes = [
         u8p, f32p, u8p, f32p, i32p, I, I, I, I, i32p, I, u16p]
@@ -200,6 +204,31 @@ def gemm_nt_acc_rows(A, SFA, B, SFB, C, M, N, K, rows, threads=1, want_acc=False
             _ptr(A, ctypes.c_uint8), _ptr(SFA, ctypes.c_float),
             _ptr(B, ctypes.c_uint8), _ptr(SFB, ctypes.c_float),
             _ptr(C, ctypes.c_float), M, N, K,
+            _ptr(chunk, ctypes.c_int), len(chunk),
+            _ptr(D[chunk_start:], ctypes.c_uint16),
+            _ptr(acc[chunk_start:], ctypes.c_double) if want_acc else None)
+
+    _run_chunks(rows, threads, run)
+    return (D, acc) if want_acc else D
+
+
+def ue8m0_to_f64(e: int, lib=None) -> float:
+    return (lib or _load()).oracle_ue8m0_to_f64(int(e) & 0xFF)
+
+
+def gemm_nt_ue8m0_rows(A, SFA_e, B, SFB_e, M, N, K, rows, threads=1, want_acc=False, lib=None):
+    """Rows ``rows`` of the plain product with UE8M0 exponent-byte scales
+    (SFA_e uint8 [K/128][round_up(M,4)], SFB_e uint8 [ceil(N/128)][K/128])."""
+    lib = lib or _load()
+    A, B, SFA_e, SFB_e = _u8(A), _u8(B), _u8(SFA_e), _u8(SFB_e)
+    rows = _i32(rows)
+    D = np.empty((len(rows), N), np.uint16)
+    acc = np.empty((len(rows), N), np.float64) if want_acc else None
+
+    def run(chunk_start, chunk):
+        lib.oracle_gemm_nt_ue8m0_rows(
+            _ptr(A, ctypes.c_uint8), _ptr(SFA_e, ctypes.c_uint8),
+            _ptr(B, ctypes.c_uint8), _ptr(SFB_e, ctypes.c_uint8), M, N, K,
             _ptr(chunk, ctypes.c_int), len(chunk),
             _ptr(D[chunk_start:], ctypes.c_uint16),
             _ptr(acc[chunk_start:], ctypes.c_double) if want_acc else None)

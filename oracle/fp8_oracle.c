@@ -18,6 +18,11 @@
  *
  *   D(m,n)    = bf16_rne(C(m,n) + acc(m,n))
  *
+ * and, with power-of-two scales stored as UE8M0 exponent bytes
+ * (oracle_gemm_nt_ue8m0_rows; same granularity and layouts, one byte each),
+ *
+ *   acc(m,n)  = sum_k 2^(ea[k][m] - 127) * 2^(eb[n/128][k] - 127) * S_k(m,n)
+ *
  * Sources (page title, section):
  *   - DeepGEMM fp8_gemm.cuh, fp8_gemm_kernel, the math warp-groups: each
  *     128-wide K block is accumulated on its own (the MMA overwrites a fresh
@@ -32,6 +37,11 @@
  *   - TCGen05 Copy Instruction (Gluon tutorial), the matmul-accumulate
  *     example: the fp32 addend C is placed in the accumulator first and the
  *     product of A and B is accumulated on top of it, so D = A B^T + C.
+ *   - TCGen05 Copy Instruction (Gluon tutorial), the closing section on
+ *     block-scaled MMA: its scales are supplied through tensor memory; the
+ *     hardware form of such scales is the 8-bit exponent-only UE8M0 format
+ *     of the OCP microscaling (MX) specification: value 2^(e - 127), and
+ *     e = 255 is NaN.
  *   - the grouped layouts (contiguous: one group index per row; masked: a
  *     per-group valid-row count, rows beyond it untouched) follow the same
  *     file's GemmType::GroupedContiguous / GroupedMasked descriptor shapes.
@@ -292,6 +302,50 @@ void oracle_gemm_nt_acc_rows(const uint8_t *A, const float *SFA, const uint8_t *
             if (acc_rows)
                 acc_rows[(long)i * N + n] = v;
             D_rows[(long)i * N + n] = oracle_f64_to_bf16_rne(v);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* UE8M0 scale byte: an unsigned biased exponent, value 2^(e - 127); 0xFF is
+ * NaN.  Every other value is exact in fp64 (and in fp32: 2^-127 is a
+ * binary32 subnormal).                                                      */
+double oracle_ue8m0_to_f64(uint8_t e)
+{
+    if (e == 0xFF)
+        return NAN;
+    return ldexp(1.0, (int)e - 127);
+}
+
+/* Plain GEMM with UE8M0 scales: SFA_e [K/128][round_up(M, 4)] and SFB_e
+ * [ceil(N/128)][K/128] hold exponent bytes instead of fp32 values; the
+ * definition is otherwise the plain one.  Only the listed rows are
+ * evaluated; acc_rows (optional) receives the unrounded values.             */
+void oracle_gemm_nt_ue8m0_rows(const uint8_t *A, const uint8_t *SFA_e, const uint8_t *B,
+                               const uint8_t *SFB_e, int M, int N, int K,
+                               const int *rows, int nrows, uint16_t *D_rows,
+                               double *acc_rows)
+{
+    long ld = sfa_ld_of(M);
+    int kb = K / 128;
+    for (int i = 0; i < nrows; ++i) {
+        int m = rows[i];
+        for (int n = 0; n < N; ++n) {
+            const uint8_t *a_row = A + (long)m * K;
+            const uint8_t *b_row = B + (long)n * K;
+            double acc = 0.0;
+            for (int k = 0; k < kb; ++k) {
+                double s_k = 0.0;
+                for (int t = 0; t < 128; ++t)
+                    s_k += e4m3_value[a_row[128 * k + t]] *
+                           e4m3_value[b_row[128 * k + t]];
+                double scale = oracle_ue8m0_to_f64(SFA_e[(long)k * ld + m]) *
+                               oracle_ue8m0_to_f64(SFB_e[(long)(n / 128) * kb + k]);
+                acc += scale * s_k;
+            }
+            if (acc_rows)
+                acc_rows[(long)i * N + n] = acc;
+            D_rows[(long)i * N + n] = oracle_f64_to_bf16_rne(acc);
         }
     }
 }

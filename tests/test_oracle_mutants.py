@@ -34,6 +34,10 @@ MUTANTS = {
     "acc_addend_subtracted": ("double v = (double)C[(long)m * N + n] +", "double v = -(double)C[(long)m * N + n] +"),
     "acc_addend_rounded_to_bf16_first": ("double v = (double)C[(long)m * N + n] +",
                                          "double v = oracle_bf16_to_f64(oracle_f64_to_bf16_rne((double)C[(long)m * N + n])) +"),
+    "ue8m0_bias_126": ("return ldexp(1.0, (int)e - 127);", "return ldexp(1.0, (int)e - 126);"),
+    "ue8m0_sfb_by_row_block": ("oracle_ue8m0_to_f64(SFB_e[(long)(n / 128) * kb + k])",
+                               "oracle_ue8m0_to_f64(SFB_e[(long)(m / 128 % ((N + 127) / 128)) * kb + k])"),
+    "ue8m0_max_not_nan": ("    if (e == 0xFF)\n        return NAN;\n    return ldexp", "    return ldexp"),
     "contiguous_ignores_group": ("const uint8_t *Bg = B + (long)g * N * K;\n        const float *SFBg = SFB + (long)g * nb * kb;",
                                  "const uint8_t *Bg = B;\n        const float *SFBg = SFB;"),
 }
@@ -58,6 +62,9 @@ def _pins():
         ("acc_zero_addend", lambda lib: pins.test_acc_zero_addend_equals_plain(lib)),
         ("acc_zero_product", lambda lib: pins.test_acc_zero_product_rounds_the_addend_like_library(lib)),
         ("acc_exact_integer", lambda lib: pins.test_acc_exact_integer_closed_form(6, 256, 512, lib)),
+        ("ue8m0_decode", lambda lib: pins.test_ue8m0_decode_exhaustive(lib)),
+        ("ue8m0_vs_fp32", lambda lib: pins.test_ue8m0_reduces_to_fp32_scales(lib)),
+        ("ue8m0_exact", lambda lib: pins.test_ue8m0_exact_integer_closed_form(6, 256, 512, lib)),
     ]
 
 

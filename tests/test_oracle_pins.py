@@ -299,6 +299,57 @@ def test_acc_exact_integer_closed_form(M, N, K, lib=None):
     assert np.array_equal(D, torch_bf16_bits(exact.astype(np.float32)))
 
 
+# ---------------------------------------------------------------- UE8M0 scales
+
+def test_ue8m0_decode_exhaustive(lib=None):
+    """Every UE8M0 byte against the MX format's closed form 2^(e - 127)
+    (Python's ldexp, not the oracle's); 0xFF is NaN."""
+    import math
+    for e in range(255):
+        assert oracle.ue8m0_to_f64(e, lib=lib) == math.ldexp(1.0, e - 127), e
+    assert math.isnan(oracle.ue8m0_to_f64(255, lib=lib))
+
+
+def test_ue8m0_reduces_to_fp32_scales(lib=None):
+    """With the exponent bytes decoded to fp32 outside the oracle (numpy
+    ldexp), the fp32-scale oracle must give the same values and bits: the
+    UE8M0 form reads the same layouts with the same indices."""
+    p = wl.make_nt_ue8m0(70, 300, 384, seed=16)
+    dec = lambda e: np.ldexp(np.float32(1.0), e.astype(np.int32) - 127).astype(np.float32)  # noqa: E731
+    rows = np.arange(p.M, dtype=np.int32)
+    D, acc = oracle.gemm_nt_ue8m0_rows(p.A, p.SFA, p.B, p.SFB, p.M, p.N, p.K, rows,
+                                       want_acc=True, lib=lib)
+    D32, acc32 = oracle.gemm_nt(p.A, dec(p.SFA), p.B, dec(p.SFB), p.M, p.N, p.K, want_acc=True, lib=lib)
+    assert np.array_equal(acc, acc32) and np.array_equal(D, D32)
+
+
+@pytest.mark.parametrize("M,N,K", [(6, 256, 512), (5, 384, 1024)])
+def test_ue8m0_exact_integer_closed_form(M, N, K, lib=None):
+    """Small integers with UE8M0 exponents 124..130: the exact value from
+    integer arithmetic, rounded once by the library's fp32 -> bf16 cast."""
+    p = wl.exact_integer_problem(M, N, K, seed=6)
+    kb, nb = K // 128, (N + 127) // 128
+    ea = (wl.raw_u64(wl.stream_key(6, 17), 0, M * kb) % np.uint64(7)).astype(np.int64) + 124
+    eb = (wl.raw_u64(wl.stream_key(6, 18), 0, nb * kb) % np.uint64(7)).astype(np.int64) + 124
+    SFA = np.full((kb, (M + 3) // 4 * 4), 127, np.uint8)
+    SFA[:, :M] = ea.reshape(M, kb).T
+    SFB = eb.reshape(nb, kb).astype(np.uint8)
+    D, acc = oracle.gemm_nt_ue8m0_rows(p.A, SFA, p.B[0], SFB, M, N, K, np.arange(M, dtype=np.int32),
+                                       want_acc=True, lib=lib)
+    va, vb = p.meta["va"], p.meta["vb"][0]
+    exact = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            tot = Fraction(0)
+            for k in range(kb):
+                s = int(np.dot(va[m, 128 * k:128 * (k + 1)], vb[n, 128 * k:128 * (k + 1)]))
+                tot += Fraction(2) ** (int(ea[m * kb + k]) - 127 + int(eb[(n // 128) * kb + k]) - 127) * s
+            exact[m, n] = float(tot)
+    assert np.array_equal(acc, exact)
+    assert np.array_equal(exact.astype(np.float32).astype(np.float64), exact)
+    assert np.array_equal(D, torch_bf16_bits(exact.astype(np.float32)))
+
+
 # ---------------------------------------------------------------- invariants
 
 def _block_partial(p, m, n, k, g=0):

@@ -81,3 +81,27 @@ def test_addend_recipe():
     assert 0.9 * np.sqrt(K) < p.C.std() < 1.1 * np.sqrt(K)
     assert p.flops() == q.flops()
     assert p.algorithmic_bytes() == q.algorithmic_bytes() + 4 * M * N
+
+
+def test_ue8m0_quantise_recipe():
+    """Power-of-two scales: each is the smallest 2^j with amax / 2^j <= 448,
+    so no block saturates and its largest element lands in the top binade
+    [224, 448]; a zero block gets the byte 127 (scale 1)."""
+    x = wl.normal_f32(0, 70, 8 * 512).reshape(8, 512) * np.float32(3.7)
+    x[3, 128:256] = 0
+    q, e = wl.quantize_rows_1x128_ue8m0(x)
+    assert e.dtype == np.uint8 and e.shape == (8, 4) and e[3, 1] == 127
+    scale = np.ldexp(1.0, e.astype(np.int64) - 127)
+    amax = np.abs(x.reshape(8, 4, 128)).astype(np.float64).max(axis=2)
+    live = amax > 0
+    assert (amax[live] / scale[live] <= 448).all() and (amax[live] / scale[live] > 224).all()
+    deq = torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64).numpy().reshape(8, 4, 128)
+    top = np.abs(deq).max(axis=2)
+    assert ((top[live] >= 224) & (top[live] <= 448)).all()
+    # the byte rule at exact powers of two: amax = 448 * 2^j gives j itself
+    assert list(wl.ue8m0_exponents(np.array([448.0, 896.0, 224.0, 448.0 * 2 ** -20, 0.0]))) == \
+        [127, 128, 126, 107, 127]
+    p = wl.make_nt_ue8m0(130, 200, 384, seed=4)
+    assert p.kind == "nt_ue8m0" and p.SFA.dtype == np.uint8 and p.SFB.shape == (1, 2, 3)
+    assert (p.SFA[:, 130:] == 127).all()
+    assert p.algorithmic_bytes() == 130 * (384 + 3 + 2 * 200) + 200 * 384 + 2 * 3

@@ -23,6 +23,10 @@ Recipe (every workload, seed 0 unless a test says otherwise):
   multiple of 128; counts (masked): uniform integers in [0, M_max].
 * The fp32 addend C of the accumulate variant: sqrt(K) * N(0,1), the spread
   of the product itself (a sum of K products of two N(0,1) values).
+* Power-of-two (UE8M0) scales: the same blocks, with scale = 2^j for the
+  smallest integer j such that amax / 2^j <= 448 (amax / 448 formed in fp64),
+  stored as the byte e = 127 + j (clamped to 0..254); a zero block gets e = 127.
+  q = e4m3(x / 2^j), where the division is exact.
 
 Layouts (all C-contiguous):
   A    uint8 [rows][K]          masked: [G][M_max][K]
@@ -185,6 +189,38 @@ def quantize_blocks_128x128(x: np.ndarray):
     return e4m3_encode(y), scale
 
 
+def ue8m0_exponents(amax: np.ndarray) -> np.ndarray:
+    """UE8M0 bytes e = 127 + j, j the smallest integer with amax / 2^j <= 448
+    (amax / 448 in fp64); 127 where amax is 0."""
+    r = np.asarray(amax, np.float64) / E4M3_MAX
+    f, E = np.frexp(np.where(r > 0, r, 1.0))      # r = f * 2^E, f in [0.5, 1)
+    j = np.where(f == 0.5, E - 1, E)              # 2^j >= r, and 2^(j-1) < r
+    e = np.where(r > 0, 127 + j, 127)
+    return np.clip(e, 0, 254).astype(np.uint8)
+
+
+def quantize_rows_1x128_ue8m0(x: np.ndarray):
+    """x: fp32 [rows][K] -> (codes uint8 [rows][K], UE8M0 bytes [rows][K/128])."""
+    rows, K = x.shape
+    xb = x.reshape(rows, K // 128, 128)
+    e = ue8m0_exponents(np.abs(xb).max(axis=2))
+    scale = np.ldexp(np.float32(1.0), e.astype(np.int32) - 127).astype(np.float32)
+    y = (xb / scale[:, :, None]).astype(np.float32)
+    return e4m3_encode(y).reshape(rows, K), e
+
+
+def quantize_blocks_128x128_ue8m0(x: np.ndarray):
+    """x: fp32 [N][K] -> (codes uint8 [N][K], UE8M0 bytes [ceil(N/128)][K/128])."""
+    N, K = x.shape
+    kb, nb = K // 128, (N + 127) // 128
+    pad = nb * 128 - N
+    xp = np.concatenate([x, np.zeros((pad, K), np.float32)]) if pad else x
+    e = ue8m0_exponents(np.abs(xp.reshape(nb, 128, kb, 128)).max(axis=(1, 3)))
+    scale = np.ldexp(np.float32(1.0), e.astype(np.int32) - 127).astype(np.float32)
+    full = np.repeat(np.repeat(scale, 128, axis=0), 128, axis=1)[:N]
+    return e4m3_encode((x / full).astype(np.float32)), e
+
+
 def sfa_ld(rows: int) -> int:
     return (rows + 3) // 4 * 4
 
@@ -214,6 +250,7 @@ class Problem:
     m_indices: np.ndarray | None = None   # contiguous, int32 [M_total]
     masked_m: np.ndarray | None = None    # masked, int32 [G]
     C: np.ndarray | None = None           # nt_acc: fp32 addend [M][N]
+    # nt_ue8m0: SFA and SFB hold UE8M0 exponent bytes (uint8) instead of fp32
     name: str = ""
     meta: dict = field(default_factory=dict)
 
@@ -240,12 +277,16 @@ class Problem:
     def flops(self) -> int:
         return 2 * self.valid_rows() * self.N * self.K
 
+    @property
+    def scale_bytes(self) -> int:
+        return 1 if self.kind == "nt_ue8m0" else 4
+
     def algorithmic_bytes(self) -> int:
         """A + SFA + B + SFB + D (+ the group layout, + C), valid rows only;
         a group's B counts once if the group has any valid row."""
-        kb, nb, N, K = self.kb, self.nb, self.N, self.K
+        kb, nb, N, K, sb = self.kb, self.nb, self.N, self.K, self.scale_bytes
         rows = self.valid_rows()
-        per_row = K + 4 * kb + 2 * N
+        per_row = K + sb * kb + 2 * N
         if self.kind == "masked":
             live = int((self.masked_m > 0).sum())
             return rows * per_row + live * (N * K + 4 * nb * kb) + 4 * self.G
@@ -253,7 +294,7 @@ class Problem:
             live = len(set(int(g) for g in np.unique(self.m_indices) if 0 <= g < self.G))
             return rows * per_row + live * (N * K + 4 * nb * kb) + 4 * self.M
         c_bytes = 4 * rows * N if self.C is not None else 0
-        return rows * per_row + N * K + 4 * nb * kb + c_bytes
+        return rows * per_row + N * K + sb * nb * kb + c_bytes
 
 
 def _quant_A(x: np.ndarray):
@@ -276,6 +317,19 @@ def make_nt_acc(M: int, N: int, K: int, seed: int = 0, name: str = "") -> Proble
     p.kind = "nt_acc"
     p.C = (normal_f32(seed, STREAM_C, M * N) * np.float32(math.sqrt(K))).reshape(M, N)
     return p
+
+
+def make_nt_ue8m0(M: int, N: int, K: int, seed: int = 0, name: str = "") -> Problem:
+    """The plain problem's A and B values with power-of-two scales: SFA and
+    SFB hold UE8M0 bytes, SFA M-major [K/128][round_up(M,4)] (pad 127)."""
+    a = normal_f32(seed, STREAM_A, M * K).reshape(M, K)
+    b = normal_f32(seed, STREAM_B, N * K).reshape(N, K)
+    qa, ea = quantize_rows_1x128_ue8m0(a)
+    qb, eb = quantize_blocks_128x128_ue8m0(b)
+    sfa = np.full((K // 128, sfa_ld(M)), 127, np.uint8)
+    sfa[:, :M] = ea.T
+    return Problem("nt_ue8m0", M, N, K, 1, qa, sfa, qb.reshape(1, N, K), eb.reshape(1, *eb.shape),
+                   name=name or f"ue8m0_{M}x{N}x{K}")
 
 
 def make_contiguous(group_rows, N: int, K: int, seed: int = 0, name: str = "") -> Problem:
