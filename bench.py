@@ -2,24 +2,36 @@
 
 One step = one pass of the hot path over the dense workload pair
 (4096 x 7168 x 2048 and 4096 x 24576 x 1536, E4M3 with 1x128 / 128x128 fp32
-scales, bf16 out): both GEMMs, each launched through the C ABI.  The metric
-is TFLOP/s over the step (2*M*N*K per GEMM).  The GEMMs run back to back on
-one stream, one CUDA-event pair around the K timed steps; each workload's
-inputs rotate over R device copies, with R chosen so that the bytes the other
-launches stream through L2 between two uses of a copy exceed twice the L2 size
-(so every launch reads inputs that are no longer in L2).  The per-kernel
-durations (the roofline's and the per-shape lines') come from a second timed
-region per workload: K launches of that GEMM alone, back to back, between one
-event pair on its stream (events between launches would serialise them).
+scales, bf16 out): both GEMMs, each launched through the C ABI.  The headline
+metric is TFLOP/s over the step (2*M*N*K per GEMM).  The GEMMs run back to
+back on one stream, one CUDA-event pair around the K timed steps; each
+workload's inputs rotate over R device copies, with R chosen so that the
+bytes the other launches stream through L2 between two uses of a copy exceed
+twice the L2 size (so every launch reads inputs that are no longer in L2).
+
+Every configuration of the method's evaluation is also measured in the same
+run, each in a timed region of its own (``shapes``): the 128 x 256 x 512
+latency case, the dense pair, small M (64 and 128 x 7168 x 16384), the
+contiguous grouped workload (8 groups, N 4096, K 7168) and the masked one (16
+groups of up to 256 rows, N 7168, K 2048).  Each shape is launched at least
+200 times back to back over its rotating copies, twice: eagerly through the C
+ABI (``ms_eager``) and replayed from one CUDA graph of the same launches
+(``ms``, which the shape's roofline uses: the device time without the
+host's per-call cost).  Each shape line carries its roofline (tensor-bound
+shapes against the fp8 peak, HBM-bound ones against the copy bandwidth) and
+its parity: the output the timed launches left in D against the CPU oracle on
+sampled rows (all rows of the small shapes).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME]
+                  [--workload NAME] [--headline-only]
 
 --workload picks another single workload (the other entries of
-workloads.WORKLOADS) for measurement runs; the default is the dense pair.
+workloads.WORKLOADS) as the headline; the default is the dense pair.
 --impl reference times the CPU oracle on the host cores over a bounded sample
-of the same workload.  Under torchrun every rank runs the same workload on its
-own GPU (independent replicas); rank 0 prints one JSON line.
+of the same workload.  --gpus N with N > 1 runs N ranks (this script
+re-launches itself under torch.distributed.run when it was not started that
+way); every rank runs the same workload on its own GPU (independent
+replicas), and rank 0 prints one JSON line.
 """
 from __future__ import annotations
 
@@ -42,8 +54,22 @@ import workloads as wl
 
 METRIC = "FP8 block-scaled GEMM TFLOPS (% of GB300 FP8 peak); GB/s at small M"
 DEFAULT_PAIR = ["dense_4096x7168x2048", "dense_4096x24576x1536"]
+# every configuration of the method's evaluation, in the order the shapes
+# lines list them
+ALL_SHAPES = ["single_128x256x512", "dense_4096x7168x2048", "dense_4096x24576x1536",
+              "smallm_64x7168x16384", "smallm_128x7168x16384",
+              "contiguous_g8_n4096_k7168", "masked_g16_m256_n7168_k2048"]
 FP8_OVER_BF16 = 2.0      # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
+FP8_NOMINAL_TFLOPS = 4500.0   # GB300 nominal dense FP8 (no sparsity)
 HBM_BOUND = {"smallm_64x7168x16384", "smallm_128x7168x16384", "masked_g16_m256_n7168_k2048"}
+LATENCY_BOUND = {"single_128x256x512"}
+MIN_SHAPE_LAUNCHES = 200
+
+
+def bound_of(name):
+    if name in LATENCY_BOUND:
+        return "latency"
+    return "hbm" if name in HBM_BOUND else "tensor"
 
 
 def log(*a):
@@ -174,7 +200,7 @@ class ClockSampler:
 class GemmCase:
     """One workload resident on the device, callable through the C ABI."""
 
-    def __init__(self, name, device, dist_rank=0, l2_bytes=0):
+    def __init__(self, name, device, dist_rank=0, l2_bytes=0, e2e=False):
         import torch
         from tests import gpu_util as gu
         self.name = name
@@ -191,15 +217,17 @@ class GemmCase:
         self.ws = gu.workspace_for(self.p, device)
         self.flops = self.p.flops()
         self.bytes = self.p.algorithmic_bytes()
-        # pinned host copies for the end-to-end measurement; two device input
-        # sets (copies 0 and 1) and two outputs let consecutive steps overlap
-        self.host = {k: v.cpu().pin_memory() for k, v in self.t.items()}
-        self.D_host = [torch.empty(self.D.shape, dtype=self.D.dtype).pin_memory() for _ in range(2)]
-        self.D2 = [self.D, torch.empty_like(self.D)]
-        self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.host.values())
+        self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.t.values())
         self.d2h_bytes = self.D.numel() * self.D.element_size()
+        if e2e:
+            # pinned host copies for the end-to-end measurement; two device
+            # input sets (copies 0 and 1) and two outputs let consecutive
+            # steps overlap
+            self.host = {k: v.cpu().pin_memory() for k, v in self.t.items()}
+            self.D_host = [torch.empty(self.D.shape, dtype=self.D.dtype).pin_memory() for _ in range(2)]
+            self.D2 = [self.D, torch.empty_like(self.D)]
         if dist_rank == 0:
-            log(f"[bench] {name}: inputs ready in {time.time() - t0:.1f}s")
+            log(f"[bench] {name}: inputs ready in {time.time() - t0:.1f}s ({self.copies} copies)")
 
     def launch(self, stream=None, step=0):
         from tests import gpu_util as gu
@@ -219,22 +247,98 @@ class GemmCase:
         self.D_host[buf].copy_(self.D2[buf], non_blocking=True)
 
 
+def _launch_all(fg, case, stream, n, offset=0):
+    for s in range(n):
+        st = case.launch(stream, offset + s)
+        if st != 0:
+            raise fg.Fp8GemmError(st, case.name)
+
+
+def time_shape(fg, case, stream, n, dist, device):
+    """Per-launch device time of one workload alone: n launches back to back
+    over its rotating copies, (1) eagerly through the C ABI and (2) replayed
+    from one CUDA graph that captured the same n launches.  One CUDA-event
+    pair on the launching stream around each batch.  Returns (graph ms or
+    None, eager ms) per launch, max over ranks."""
+    import torch
+    _launch_all(fg, case, stream, 3)
+    e_a = torch.cuda.Event(enable_timing=True)
+    e_b = torch.cuda.Event(enable_timing=True)
+    e_a.record(stream)
+    _launch_all(fg, case, stream, n)
+    e_b.record(stream)
+    torch.cuda.synchronize()
+    eager = max_over_ranks(dist, e_a.elapsed_time(e_b), device) / n
+    fg.check(fg.fp8_gemm_get_device_error(), f"{case.name} eager timing")
+
+    graph_ms = None
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(device)
+    side.wait_stream(stream)
+    with torch.cuda.graph(g, stream=side):
+        _launch_all(fg, case, side, n)
+    stream.wait_stream(side)
+    with torch.cuda.stream(stream):
+        g.replay()                       # warm-up replay
+        e_a.record(stream)
+        g.replay()
+        e_b.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = max_over_ranks(dist, e_a.elapsed_time(e_b), device) / n
+    fg.check(fg.fp8_gemm_get_device_error(), f"{case.name} graph timing")
+    del g
+    return graph_ms, eager
+
+
+def roofline_entry(case, ms, peaks):
+    """The shape's position against its roofline.  t_roof is the slower of
+    the FLOPs at the fp8 tensor peak and the algorithmic bytes at the copy
+    bandwidth; frac_roofline = t_roof / t."""
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    tflops = case.flops / (ms / 1e3) / 1e12
+    gbs = case.bytes / (ms / 1e3) / 1e9
+    t_roof = max(case.flops / (fp8_peak * 1e12), case.bytes / (peaks["hbm_gbs"] * 1e9))
+    bound = bound_of(case.name)
+    e = {"workload": case.name, "bound": bound, "ms": ms, "us": ms * 1e3, "tflops": tflops, "gbs": gbs,
+         "frac_roofline": t_roof / (ms / 1e3), "frac_fp8_peak": tflops / fp8_peak,
+         "frac_fp8_nominal": tflops / FP8_NOMINAL_TFLOPS, "frac_hbm": gbs / peaks["hbm_gbs"],
+         "flops": case.flops, "algorithmic_bytes": case.bytes, "traffic": load_traffic(case.name)}
+    if bound == "hbm":
+        e.update(achieved=gbs, peak=peaks["hbm_gbs"], unit="GB/s", frac=gbs / peaks["hbm_gbs"])
+    elif bound == "tensor":
+        e.update(achieved=tflops, peak=fp8_peak, unit="TFLOP/s", frac=tflops / fp8_peak)
+    else:
+        e.update(achieved=ms * 1e3, peak=None, unit="us", frac=None)
+    if case.p.kind == "contiguous":
+        e["sum_m"] = int(case.p.M)
+    if case.p.kind == "masked":
+        e["sum_m"] = int(np.clip(case.p.masked_m, 0, case.p.M).sum())
+    return e
+
+
 def run_ours(args, dist, ws, rank, local):
     import torch
     import fp8_block_scaled_persistent_gb300 as fg
 
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py (--impl ours) needs a CUDA device")
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     fg.library()
-    names = DEFAULT_PAIR if args.workload == "dense_pair" else [args.workload]
+    headline = DEFAULT_PAIR if args.workload == "dense_pair" else [args.workload]
+    if args.headline_only or args.workload != "dense_pair":
+        shape_names = list(headline)
+    else:
+        shape_names = list(ALL_SHAPES)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    cases = [GemmCase(n, device, rank, l2) for n in names]
+    by_name = {}
+    for n in dict.fromkeys(headline + shape_names):
+        by_name[n] = GemmCase(n, device, rank, l2, e2e=n in headline)
+    cases = [by_name[n] for n in headline]
     stream = torch.cuda.current_stream(device)
 
-    def step(s, only=None):
-        for i, c in enumerate(cases):
-            if only is not None and i != only:
-                continue
+    def step(s):
+        for c in cases:
             st = c.launch(stream, s)
             if st != 0:
                 raise fg.Fp8GemmError(st, c.name)
@@ -260,29 +364,20 @@ def run_ours(args, dist, ws, rank, local):
     region1.record(stream)
     torch.cuda.synchronize()
     wall = time.time() - wall0
-    if sampler:
-        sampler.mark_end()
     barrier(dist)
-    clocks = sampler.stop() if sampler else None
     fg.check(fg.fp8_gemm_get_device_error(), "timed steps")
-
     total_ms = max_over_ranks(dist, region0.elapsed_time(region1), device)
 
-    # per-kernel durations: each workload alone, back to back, one event pair
-    per_case_n = max(8, min(args.steps, 400))
-    per_case_ms = []
-    for i, c in enumerate(cases):
-        for s in range(2):
-            step(s, only=i)
-        e_a = torch.cuda.Event(enable_timing=True)
-        e_b = torch.cuda.Event(enable_timing=True)
-        e_a.record(stream)
-        for s in range(per_case_n):
-            step(s, only=i)
-        e_b.record(stream)
-        torch.cuda.synchronize()
-        per_case_ms.append([max_over_ranks(dist, e_a.elapsed_time(e_b), device) / per_case_n])
-    fg.check(fg.fp8_gemm_get_device_error(), "per-kernel timing")
+    # per-shape device times: each workload alone, at least MIN_SHAPE_LAUNCHES
+    # launches back to back (eager, and replayed from a CUDA graph)
+    per_n = max(MIN_SHAPE_LAUNCHES, min(args.steps, 2000))
+    timed = {}
+    for n in shape_names:
+        timed[n] = time_shape(fg, by_name[n], stream, per_n, dist, device)
+    if sampler:
+        sampler.mark_end()
+    clocks = sampler.stop() if sampler else None
+
     ms_per_step = total_ms / args.steps
     flops_step = sum(c.flops for c in cases)
     bytes_step = sum(c.bytes for c in cases)
@@ -339,49 +434,47 @@ def run_ours(args, dist, ws, rank, local):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1), device)
     e2e_value = sum_over_ranks(dist, flops_step * e2e_steps, device) / (e2e_ms / 1e3) / 1e12
+    fg.check(fg.fp8_gemm_get_device_error(), "end-to-end steps")
 
     peaks = load_peaks()
-    hbm = args.workload in HBM_BOUND
-    # dominant kernel: the case with the largest share of device time
-    i_dom = int(np.argmax([sum(x) for x in per_case_ms]))
-    dom = cases[i_dom]
-    dom_ms = statistics.mean(per_case_ms[i_dom])
-    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
-    traffic = load_traffic(dom.name)
-    if hbm:
-        achieved = dom.bytes / (dom_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                "kernel": f"fp8_gemm_kernel ({dom.name})",
-                "peak_source": f"{peaks['source']} HBM copy bandwidth"}
-    else:
-        achieved = dom.flops / (dom_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                "frac": achieved / fp8_peak, "traffic": traffic,
-                "kernel": f"fp8_gemm_kernel ({dom.name})",
-                "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16} (nominal fp8/bf16)"}
     shapes = []
-    for i, c in enumerate(cases):
-        ms = statistics.mean(per_case_ms[i])
-        shapes.append({"workload": c.name, "ms": ms, "tflops": c.flops / (ms / 1e3) / 1e12,
-                       "gbs": c.bytes / (ms / 1e3) / 1e9,
-                       "frac_fp8_peak": c.flops / (ms / 1e3) / 1e12 / fp8_peak,
-                       "frac_hbm": c.bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]})
+    for n in shape_names:
+        graph_ms, eager_ms = timed[n]
+        e = roofline_entry(by_name[n], graph_ms if graph_ms is not None else eager_ms, peaks)
+        e["ms_eager"] = eager_ms
+        e["launches"] = per_n
+        e["timing"] = "CUDA graph replay" if graph_ms is not None else "eager"
+        shapes.append(e)
+    # the dominant kernel of the headline step: the case with the largest
+    # share of device time, its per-launch time from its own timed region
+    head = [e for e in shapes if e["workload"] in headline] or \
+        [roofline_entry(c, ms_per_step, peaks) for c in cases]
+    dom = max(head, key=lambda e: e["ms"])
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    roof = {"bound": dom["bound"], "achieved": dom["achieved"], "peak": dom["peak"], "unit": dom["unit"],
+            "frac": dom["frac"], "traffic": dom["traffic"], "kernel": f"fp8_gemm_kernel ({dom['workload']})",
+            "ms_per_launch": dom["ms"],
+            "peak_source": (f"{peaks['source']} HBM copy bandwidth" if dom["bound"] == "hbm" else
+                            f"{peaks['source']} bf16 burst x {FP8_OVER_BF16} (nominal fp8/bf16)")}
+    if dom["bound"] == "tensor":
+        roof["frac_fp8_nominal"] = dom["frac_fp8_nominal"]
     out = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-        "config": {"workload": "+".join(names), "accumulate": "f32 per 128-K block, promoted in f32",
+        "config": {"workload": "+".join(headline), "accumulate": "f32 per 128-K block, promoted in f32",
                    "output": "bf16", "seed": 0,
                    "l2": "inputs larger than L2: each workload's inputs rotate over "
-                         + ", ".join(f"{c.copies}" for c in cases)
+                         + ", ".join(f"{by_name[n].copies}" for n in headline)
                          + " device copies, more than 2 x L2 streamed between two uses of a copy; no flush",
-                   "per_kernel_timing": f"{per_case_n} launches of each workload alone, back to back, "
-                                        "between one CUDA-event pair on its stream",
+                   "per_shape_timing": f"{per_n} launches of each workload alone, back to back over its "
+                                       "rotating copies, between one CUDA-event pair on its stream: replayed "
+                                       "from one CUDA graph (ms) and eagerly through the C ABI (ms_eager)",
                    **({"addend": "fp32 C [M][N], added once (fp8_gemm_nt_accumulate)"}
                       if any(c.p.C is not None for c in cases) else {}),
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "flops_per_step": flops_step, "algorithmic_bytes_per_step": bytes_step},
+                   "flops_per_step": flops_step, "algorithmic_bytes_per_step": bytes_step,
+                   "fp8_peak_tflops": fp8_peak, "hbm_peak_gbs": peaks["hbm_gbs"]},
         "shapes": shapes, "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": sum(c.h2d_bytes for c in cases),
@@ -390,7 +483,7 @@ def run_ours(args, dist, ws, rank, local):
         "gpu_launches": len(cases) * args.steps,
         "clocks": clocks, "wall_s_timed_region": wall, "impl": "ours",
     }
-    return out, cases
+    return out, cases, [by_name[n] for n in shape_names]
 
 
 def load_traffic(name):
@@ -457,8 +550,8 @@ def _run_rows(oracle, p, rows, threads):
 
 
 def parity_of(cases, refs):
-    """The GPU output the timed launches left in each workload's D against
-    the oracle rows of the CPU sample, with the method's tolerance."""
+    """The GPU output the timed launches left in each headline workload's D
+    against the oracle rows of the CPU sample, with the method's tolerance."""
     from tests import gpu_util as gu
     from tests.tolerance import check
     out = {"rows": 0, "elements": 0, "max_err_over_bound": 0.0, "global_diff": 0.0, "ok": True}
@@ -478,6 +571,85 @@ def parity_of(cases, refs):
         out["elements"] += st["elements"]
         out["max_err_over_bound"] = max(out["max_err_over_bound"], st["max_err_over_bound"])
         out["global_diff"] = max(out["global_diff"], st["global_diff"])
+    return out
+
+
+def parity_rows(p, extra=24, seed=0):
+    """Rows of D to compare for one workload, as (group or None, rows):
+    every row of a problem of at most 256 rows; otherwise the first and last
+    rows, the rows on both sides of the first 128-row block boundaries and of
+    the last one, and `extra` random rows.  Contiguous: also the first and
+    last row of every group and the rows on both sides of every group
+    boundary.  Masked: per live group, its first and last valid row, the rows
+    on both sides of the 128-row boundary when the count crosses it, and a
+    few random valid rows."""
+    rng = np.random.default_rng(seed)
+    if p.kind == "masked":
+        out = []
+        for g in range(p.G):
+            c = int(min(max(int(p.masked_m[g]), 0), p.M))
+            if c == 0:
+                continue
+            rows = {0, c - 1} | ({127, 128} if c > 128 else set())
+            rows |= set(int(x) for x in rng.integers(0, c, size=min(3, c)))
+            out.append((g, np.array(sorted(r for r in rows if r < c), np.int32)))
+        return out
+    if p.M <= 256:
+        return [(None, np.arange(p.M, dtype=np.int32))]
+    must = {0, 1, 127, 128, 255, 256, p.M - 129, p.M - 128, p.M - 1}
+    if p.kind == "contiguous":
+        lay = np.asarray(p.m_indices)
+        edges = np.flatnonzero(np.diff(lay)) + 1          # first row of each later group
+        for e in edges:
+            must |= {int(e) - 1, int(e)}
+    must |= set(int(x) for x in rng.integers(0, p.M, size=extra))
+    return [(None, np.array(sorted(r for r in must if 0 <= r < p.M), np.int32))]
+
+
+def shape_parity(case, threads):
+    """The output the timed launches left in the workload's D against the
+    oracle on parity_rows, within the method's tolerance; for the masked
+    layout also that every row at or past a group's count still holds the
+    sentinel the buffer was filled with."""
+    import oracle
+    from tests import gpu_util as gu
+    from tests.tolerance import check
+    p = case.p
+    d = gu.bits(case.D)
+    out = {"rows": 0, "elements": 0, "max_err_over_bound": 0.0, "global_diff": 0.0, "ok": True}
+    try:
+        for g, rows in parity_rows(p):
+            if p.kind == "masked":
+                ref = oracle.gemm_grouped_masked_rows(p.A, p.SFA, p.B, p.SFB, p.masked_m, p.G, p.M, p.N, p.K,
+                                                      g, rows, threads=threads)
+                got = d[g][rows]
+            elif p.kind == "contiguous":
+                ref = oracle.gemm_grouped_contiguous_rows(p.A, p.SFA, p.B, p.SFB, p.m_indices, p.M, p.N, p.K,
+                                                          p.G, rows, threads=threads)
+                got = d[rows]
+            elif p.kind == "nt_acc":
+                ref = oracle.gemm_nt_acc_rows(p.A, p.SFA, p.B, p.SFB, p.C, p.M, p.N, p.K, rows,
+                                              threads=threads)
+                got = d[rows]
+            else:
+                ref = oracle.gemm_nt_rows(p.A, p.SFA, p.B, p.SFB, p.M, p.N, p.K, rows, threads=threads)
+                got = d[rows]
+            st = check(got, ref, f"{p.name} group {g}" if g is not None else p.name)
+            out["rows"] += len(rows)
+            out["elements"] += st["elements"]
+            out["max_err_over_bound"] = max(out["max_err_over_bound"], st["max_err_over_bound"])
+            out["global_diff"] = max(out["global_diff"], st["global_diff"])
+        if p.kind == "masked":
+            untouched = 0
+            for g in range(p.G):
+                c = int(min(max(int(p.masked_m[g]), 0), p.M))
+                tail = d[g][c:]
+                assert (tail == gu.SENTINEL).all(), f"{p.name}: group {g} rows past its count were written"
+                untouched += tail.shape[0]
+            out["untouched_rows_checked"] = untouched
+    except AssertionError as e:
+        out["ok"] = False
+        out["failure"] = str(e)
     return out
 
 
@@ -526,7 +698,22 @@ def run_reference(args, rank):
 
 # ----------------------------------------------------------------------------- main
 
+def relaunch_under_torchrun(argv, n):
+    """Runs this script as n ranks under torch.distributed.run on this node
+    (127.0.0.1 rendezvous, a free port) and returns its exit status."""
+    import socket
+    sock = socket.socket()
+    sock.bind(("127.0.0.1", 0))
+    port = sock.getsockname()[1]
+    sock.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__), *argv]
+    log(f"[bench] --gpus {n}: launching {n} ranks under torch.distributed.run")
+    return subprocess.call(cmd)
+
+
 def main(argv=None):
+    argv = list(sys.argv[1:] if argv is None else argv)
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -534,6 +721,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dense_pair",
                     choices=["dense_pair"] + sorted(wl.WORKLOADS))
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time only the headline workload(s), not every configuration")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of CPU oracle work for the cpu_baseline sample")
     ap.add_argument("--no-clocks", action="store_true")
@@ -541,8 +730,15 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
 
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return relaunch_under_torchrun(argv, args.gpus)
     ws, rank, local = dist_env()
+    if ws != args.gpus:
+        log(f"[bench] --gpus {args.gpus} does not match WORLD_SIZE={ws}")
+        return 2
     if args.impl == "reference":
         if rank != 0:
             return 0
@@ -550,7 +746,7 @@ def main(argv=None):
         return 0
 
     dist = init_dist(ws, "nccl")
-    out, cases = run_ours(args, dist, ws, rank, local)
+    out, cases, shape_cases = run_ours(args, dist, ws, rank, local)
     if rank == 0:
         if not args.no_cpu_baseline:
             import oracle
@@ -567,6 +763,10 @@ def main(argv=None):
             out["cpu_baseline"]["single_core"] = {
                 "value": v1, "unit": "TFLOP/s", "cores": 1, "sample": sample1, "seconds": dt1,
                 "full_step_seconds_extrapolated": sum(c.flops for c in cases) / (v1 * 1e12)}
+            # every shape's own output against the oracle
+            for e, c in zip(out["shapes"], shape_cases):
+                e["parity"] = shape_parity(c, threads)
+            out["parity"]["shapes_ok"] = all(e["parity"]["ok"] for e in out["shapes"])
         print(json.dumps(out), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -235,6 +235,10 @@ int choose_nt(int M, int N, int K, int sms, long long workspace_bytes, NtChoice 
         c.grid = P ? P : std::min(sms, c.tiles);
     };
     if (osplit > 0) {
+        // every CTA of a split schedule must be resident at once (one CTA per
+        // SM): a tile's reducer waits for the partials of the others
+        if (osplit > sms)
+            return FP8G_ERR_UNSUPPORTED;
         const int bn = obn ? obn : 128;
         const long long P = std::min<long long>(osplit, (long long)tiles_for(bn) * kb);
         if (!fits32(bn, P))

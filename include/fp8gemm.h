@@ -169,6 +169,10 @@ int fp8_gemm_sfa_ld(int M);
  *   split_ctas  : > 0 forces the split-K schedule over that many CTAs (with
  *                 128-column tiles unless block_n says 256; needs a workspace
  *                 of fp8_gemm_workspace_size_for bytes), < 0 forbids splitting.
+ *                 A forced count above the device's SM count makes the GEMM
+ *                 calls return FP8G_ERR_UNSUPPORTED: all CTAs of a split
+ *                 schedule must be resident at once (one per SM), because a
+ *                 tile's reducing CTA waits for the others' partials.
  * Returns FP8G_ERR_INVALID_ARG for values outside those sets.  The
  * environment variable FP8G_FORCE_CONFIG="block_n[,split_ctas]", read when
  * the library loads, sets the same values (a malformed value is ignored);
@@ -196,17 +200,23 @@ int fp8_gemm_set_wait_timeout_ns(uint64_t ns);
  * cannot provide the workspace the split-K schedule needs.  The paper has
  * no counterpart to this entry point.
  *
- * Same operation, layouts, requirements and schedule as fp8_gemm_nt given
- * all the workspace it asks for; the caller still passes A, SFA, B, SFB and
- * D.  The split-K scratch (counters and fp32 partials) is a static device
- * array of 24 MiB (25,165,824 bytes) inside this library, enough for the
- * schedule of any plain GEMM on a GPU with up to 190 SMs; every GPU that
- * loads the library holds it until the process exits.  Nothing is allocated per call: no cudaMalloc, no cudaFree.
+ * Same operation, layouts and requirements as fp8_gemm_nt; the caller still
+ * passes A, SFA, B, SFB and D.  The split-K scratch (counters and fp32
+ * partials) is a static device array of 24 MiB (25,165,824 bytes) inside
+ * this library; every GPU that loads the library holds it until the process
+ * exits.  Nothing is allocated per call: no cudaMalloc, no cudaFree.
+ *   - Schedule: fp8_gemm_nt's, given all the workspace it asks for, whenever
+ *     that fits the array -- always the case for the automatic tile width on
+ *     a GPU with up to 190 SMs.  When it does not fit (a forced 256-column
+ *     tile width through fp8_gemm_set_override, or a GPU with more SMs) the
+ *     call quietly takes the best automatic schedule that fits the array,
+ *     down to the unsplit one, and still returns FP8G_OK.
+ *   - Only a forced split count (fp8_gemm_set_override's split_ctas > 0)
+ *     whose scratch exceeds the array returns FP8G_ERR_SCRATCH_LIMIT, and
+ *     then nothing is launched.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.
- *   - A problem whose split-K schedule needs more scratch than the array
- *     holds returns FP8G_ERR_SCRATCH_LIMIT and launches nothing.
  *   - Every call shares the one array and clears its counters (an async
  *     memset on `stream`) before launching; calls that overlap on the GPU
  *     (different streams, or several host threads) race on it and must be

@@ -230,8 +230,12 @@ def test_full_size_sampled_rows(name):
         ref = oracle.gemm_nt_rows(p.A, p.SFA, p.B, p.SFB, p.M, p.N, p.K, rows, threads=THREADS)
         check(got[rows], ref, name)
     elif p.kind == "contiguous":
+        # every group's first and last row, the first row of the group's
+        # second 128-row block, and random rows
         starts = np.cumsum([0] + p.meta["group_rows"][:-1])
-        rows = gu.sample_rows(p.M, 10, seed=2, must=list(starts) + [p.M - 1])
+        ends = starts + np.array(p.meta["group_rows"]) - 1
+        must = list(starts) + list(ends) + [s + 128 for s in starts if s + 128 <= p.M - 1]
+        rows = gu.sample_rows(p.M, 16, seed=2, must=must)
         ref = oracle.gemm_grouped_contiguous_rows(p.A, p.SFA, p.B, p.SFB, p.m_indices, p.M, p.N,
                                                   p.K, p.G, rows, threads=THREADS)
         check(got[rows], ref, name)
@@ -239,9 +243,12 @@ def test_full_size_sampled_rows(name):
         for g in range(p.G):
             c = int(p.masked_m[g])
             assert (got[g, c:] == gu.SENTINEL).all(), f"{name}: group {g} rows beyond {c} written"
-        for g in np.nonzero(p.masked_m)[0][:6]:
+        # every live group: its first and last valid row, both sides of the
+        # 128-row boundary when the count crosses it, and random valid rows
+        for g in np.nonzero(p.masked_m)[0]:
             c = int(p.masked_m[g])
-            rows = gu.sample_rows(c, 3, seed=int(g), must=(0, c - 1))
+            must = (0, c - 1) + ((127, 128) if c > 128 else ())
+            rows = gu.sample_rows(c, 3, seed=int(g), must=must)
             ref = oracle.gemm_grouped_masked_rows(p.A, p.SFA, p.B, p.SFB, p.masked_m, p.G, p.M,
                                                   p.N, p.K, int(g), rows, threads=THREADS)
             check(got[g][rows], ref, f"{name} g{g}")
