@@ -35,7 +35,7 @@ FP8G_KIND_GROUPED_MASKED = 2
 EXPORTS = (
     "fp8_gemm_nt", "fp8_gemm_nt_accumulate", "fp8_gemm_grouped_contiguous", "fp8_gemm_grouped_masked",
     "fp8_gemm_workspace_size", "fp8_gemm_get_device_error", "fp8_gemm_status_string",
-    "fp8_gemm_sfa_ld", "fp8_gemm_set_override", "fp8_gemm_workspace_size_for",
+    "fp8_gemm_sfa_ld", "fp8_gemm_set_override", "fp8_gemm_set_pair_mode", "fp8_gemm_workspace_size_for",
     "fp8_gemm_set_wait_timeout_ns", "fp8_gemm_nt_noalloc", "fp8_gemm_version",
 )
 
@@ -79,6 +79,8 @@ def library(path: str = LIB_PATH):
         lib.fp8_gemm_sfa_ld.restype = i
         lib.fp8_gemm_set_override.argtypes = [i, i]
         lib.fp8_gemm_set_override.restype = i
+        lib.fp8_gemm_set_pair_mode.argtypes = [i]
+        lib.fp8_gemm_set_pair_mode.restype = i
         lib.fp8_gemm_set_wait_timeout_ns.argtypes = [u64]
         lib.fp8_gemm_set_wait_timeout_ns.restype = i
         lib.fp8_gemm_nt_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
@@ -172,6 +174,12 @@ def fp8_gemm_sfa_ld(M) -> int:
 
 def fp8_gemm_set_override(block_n=0, split_ctas=0) -> int:
     return library().fp8_gemm_set_override(int(block_n), int(split_ctas))
+
+
+def fp8_gemm_set_pair_mode(mode=0) -> int:
+    """1: unsplit calls run on CTA pairs (256 x 128 tiles over two SMs),
+    0: automatic choice, -1: never.  Returns the status code."""
+    return library().fp8_gemm_set_pair_mode(int(mode))
 
 
 def fp8_gemm_set_wait_timeout_ns(ns) -> int:

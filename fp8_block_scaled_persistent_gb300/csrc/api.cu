@@ -25,6 +25,9 @@ using fp8g::Params;
 
 constexpr int kVersion = 10000;          // 1.0.0
 constexpr int kDefaultSms = 152;
+// the automatic choice runs unsplit problems with at least one 256-row pair
+// tile per resident pair on CTA pairs
+constexpr bool kPairAuto = false;
 constexpr int kMaxDevices = 64;
 constexpr long long kMaxDim = 1ll << 30;  // rows, N and K limits (int32-safe indexing)
 
@@ -32,6 +35,8 @@ __device__ int g_error_word;              // sticky device-side error bits, per 
 
 std::atomic<int> g_override_bn{0};
 std::atomic<int> g_override_split{0};
+// CTA-pair kernel: 0 = automatic choice, 1 = wherever it applies, -1 = never
+std::atomic<int> g_override_pair{0};
 
 // FP8G_FORCE_CONFIG="block_n[,split_ctas]" sets the tuning overrides when the
 // library loads (the values fp8_gemm_set_override accepts); a malformed value
@@ -59,11 +64,29 @@ struct EnvOverride {
         g_override_split.store((int)split);
     }
 } g_env_override;
+
+// FP8G_PAIR_MODE="-1" | "0" | "1" sets the CTA-pair choice when the library
+// loads (the values fp8_gemm_set_pair_mode accepts); anything else is ignored.
+struct EnvPairMode {
+    EnvPairMode()
+    {
+        const char *v = std::getenv("FP8G_PAIR_MODE");
+        if (!v)
+            return;
+        if (!std::strcmp(v, "-1"))
+            g_override_pair.store(-1);
+        else if (!std::strcmp(v, "0"))
+            g_override_pair.store(0);
+        else if (!std::strcmp(v, "1"))
+            g_override_pair.store(1);
+    }
+} g_env_pair_mode;
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 
 // ------------------------------------------------------------ device facts
 
 struct DeviceInfo {
+    int id = 0;
     int sms = 0;
     int *error_word = nullptr;
 };
@@ -86,6 +109,7 @@ int current_device_info(DeviceInfo &out)
         if (cudaGetSymbolAddress(&w, g_error_word) != cudaSuccess)
             return FP8G_ERR_CUDA;
         d.error_word = static_cast<int *>(w);
+        d.id = dev;
         d.sms = sms;
     }
     out = d;
@@ -320,6 +344,62 @@ bool make_maps(LaunchArgs &a, const void *A, const float *SFA, const void *B, co
                        make_pair_map(&a.tmap_b2, B, (uint64_t)b_rows, K, (uint32_t)block_n)));
 }
 
+// The views of a CTA-pair launch: A boxes of 128 rows (each CTA its half of a
+// 256-row pair tile), B boxes of half the pair tile's columns, D panels of
+// pair_panel_cols() columns; the scale views are those of make_maps.
+bool make_pair_maps(LaunchArgs &a, const void *A, const float *SFA, const void *B, const float *SFB, void *D,
+                    long long a_rows, long long b_rows, long long d_rows, long long sfa_rows, int sfa_ld,
+                    long long sfb_count, int N, int K)
+{
+    const int pc = fp8g::pair_panel_cols();
+    std::memset(&a.tmap_a2, 0, sizeof(a.tmap_a2));
+    std::memset(&a.tmap_b2, 0, sizeof(a.tmap_b2));
+    return make_map(&a.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, a_rows, K, 128, 128,
+                    CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(&a.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, b_rows, K, 128,
+                    (uint32_t)fp8g::pair_block_n() / 2, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(&a.tmap_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, N, d_rows, (uint64_t)N * 2, pc, 32,
+                    panel_swizzle(pc)) &&
+           make_map(&a.tmap_sfa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SFA, sfa_ld, sfa_rows, (uint64_t)sfa_ld * 4,
+                    128, fp8g::kScaleChunk, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           make_map(&a.tmap_sfb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SFB, sfb_count, 0, 0, fp8g::kScaleChunk + 4, 1,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// Whether an unsplit launch runs on CTA pairs, and over how many pairs.
+// `pair_tiles` is the number of 256-row pair tiles the problem has.
+bool want_pair(long long pair_tiles, const DeviceInfo &dev, int &pairs)
+{
+    const int mode = g_override_pair.load();
+    const int obn = g_override_bn.load();
+    if (mode < 0 || (obn != 0 && obn != fp8g::pair_block_n()) || pair_tiles <= 0)
+        return false;
+    pairs = fp8g::max_active_pairs(dev.id);
+    if (pairs <= 0)
+        return false;
+    if (mode > 0)
+        return true;
+    return kPairAuto && pair_tiles >= pairs;
+}
+
+// The plain GEMM on CTA pairs (no split), with or without the addend C.
+int run_nt_pair(const void *A, const float *SFA, const void *B, const float *SFB, const float *C, void *D, int M,
+                int N, int K, int pairs, const DeviceInfo &dev, fp8g_stream_t stream)
+{
+    const int bn = fp8g::pair_block_n();
+    LaunchArgs a;
+    fill_common(a.p, M, N, K, 1, SFA, SFB, D, nullptr, bn, dev);
+    a.p.c = C;
+    a.p.num_m_blocks = ceil_div(M, 256);
+    a.p.group_m = 8;
+    a.p.num_tiles = a.p.num_m_blocks * a.p.num_n_blocks;
+    if (!make_pair_maps(a, A, SFA, B, SFB, D, M, N, M, a.p.kb, a.p.sfa_ld, (long long)a.p.nb * a.p.kb, N, K))
+        return FP8G_ERR_CUDA;
+    a.grid = 2 * std::min(pairs, a.p.num_tiles);
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    return to_status(fp8g::launch_pair(C ? fp8g::kKindNTAcc : fp8g::kKindNT, a));
+}
+
 // The plain GEMM, with or without the fp32 addend C (validated by the caller).
 int run_nt(const void *A, const float *SFA, const void *B, const float *SFB, const float *C, void *D, int M, int N,
            int K, void *workspace, size_t workspace_bytes, fp8g_stream_t stream)
@@ -334,6 +414,9 @@ int run_nt(const void *A, const float *SFA, const void *B, const float *SFB, con
         return st;
     if (c.split_ctas && !aligned(workspace, 256))
         return FP8G_ERR_MISALIGNED;
+    int pairs = 0;
+    if (!c.split_ctas && want_pair((long long)ceil_div(M, 256) * ceil_div(N, fp8g::pair_block_n()), dev, pairs))
+        return run_nt_pair(A, SFA, B, SFB, C, D, M, N, K, pairs, dev, stream);
 
     LaunchArgs a;
     fill_common(a.p, M, N, K, 1, SFA, SFB, D, nullptr, c.block_n, dev);
@@ -414,6 +497,21 @@ int fp8_gemm_grouped_contiguous(const void *A, const float *SFA, const void *B, 
     DeviceInfo dev;
     if ((st = current_device_info(dev)) != FP8G_OK)
         return st;
+    int pairs = 0;
+    if (want_pair((long long)ceil_div(M_total, 256) * ceil_div(N, fp8g::pair_block_n()), dev, pairs)) {
+        LaunchArgs a;
+        fill_common(a.p, M_total, N, K, G, SFA, SFB, D, m_indices, fp8g::pair_block_n(), dev);
+        a.p.num_m_blocks = ceil_div(M_total, 256);
+        a.p.group_m = 8;
+        const int pair_tiles = a.p.num_m_blocks * a.p.num_n_blocks;
+        a.p.num_tiles = 2 * pair_tiles;     // two passes (see the pair scheduler)
+        if (!make_pair_maps(a, A, SFA, B, SFB, D, M_total, (long long)G * N, M_total, a.p.kb, a.p.sfa_ld,
+                            (long long)G * a.p.nb * a.p.kb, N, K))
+            return FP8G_ERR_CUDA;
+        a.grid = 2 * std::min(pairs, pair_tiles);
+        a.stream = reinterpret_cast<cudaStream_t>(stream);
+        return to_status(fp8g::launch_pair(fp8g::kKindContiguous, a));
+    }
     const int mb = M_total / 128;
     const int block_n = pick_block_n(N, (long long)mb * ceil_div(N, 256) >= dev.sms);
     LaunchArgs a;
@@ -449,6 +547,20 @@ int fp8_gemm_grouped_masked(const void *A, const float *SFA, const void *B, cons
     DeviceInfo dev;
     if ((st = current_device_info(dev)) != FP8G_OK)
         return st;
+    int pairs = 0;
+    if (want_pair((long long)G * ceil_div(M_max, 256) * ceil_div(N, fp8g::pair_block_n()), dev, pairs)) {
+        LaunchArgs a;
+        fill_common(a.p, M_max, N, K, G, SFA, SFB, D, masked_m, fp8g::pair_block_n(), dev);
+        a.p.num_m_blocks = ceil_div(M_max, 256);
+        a.p.group_m = a.p.num_m_blocks;
+        const long long tiles_max = (long long)G * a.p.num_m_blocks * a.p.num_n_blocks;
+        if (!make_pair_maps(a, A, SFA, B, SFB, D, (long long)G * M_max, (long long)G * N, (long long)G * M_max,
+                            (long long)G * a.p.kb, a.p.sfa_ld, (long long)G * a.p.nb * a.p.kb, N, K))
+            return FP8G_ERR_CUDA;
+        a.grid = 2 * (int)std::min<long long>(pairs, tiles_max);
+        a.stream = reinterpret_cast<cudaStream_t>(stream);
+        return to_status(fp8g::launch_pair(fp8g::kKindMasked, a));
+    }
     const int mb = ceil_div(M_max, 128);
     const long long tiles_max256 = (long long)G * mb * ceil_div(N, 256);
     const int block_n = pick_block_n(N, tiles_max256 >= dev.sms);
@@ -534,6 +646,14 @@ int fp8_gemm_set_override(int block_n, int split_ctas)
     return FP8G_OK;
 }
 
+int fp8_gemm_set_pair_mode(int mode)
+{
+    if (mode < -1 || mode > 1)
+        return FP8G_ERR_INVALID_ARG;
+    g_override_pair.store(mode);
+    return FP8G_OK;
+}
+
 int fp8_gemm_set_wait_timeout_ns(uint64_t ns)
 {
     if (ns < 1000000ull)
@@ -614,6 +734,9 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const float *SFA, const void *
         if ((st = choose_nt(M, N, K, dev.sms, (long long)kNoAllocScratchBytes, c)) != FP8G_OK)
             return st;
     }
+    int pairs = 0;
+    if (!c.split_ctas && want_pair((long long)ceil_div(M, 256) * ceil_div(N, fp8g::pair_block_n()), dev, pairs))
+        return run_nt_pair(A, SFA, B, SFB, nullptr, D, M, N, K, pairs, dev, stream);
     const size_t counters = ((size_t)c.tiles * 8 * sizeof(int) + 255) / 256 * 256;
 
     LaunchArgs a;

@@ -76,9 +76,6 @@ constexpr int kLaunchRegs = 168;
 static_assert(128 * kRegsCtl + 256 * kRegsEpi <= kNumThreads * kLaunchRegs,
               "register reallocation exceeds the launch allocation");
 
-// kKindNTAcc: the plain GEMM with an fp32 addend, D = bf16(C + A B^T scaled)
-enum Kind : int { kKindNT = 0, kKindContiguous = 1, kKindMasked = 2, kKindNTAcc = 3 };
-
 template <int BN>
 struct Cfg {
     static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");

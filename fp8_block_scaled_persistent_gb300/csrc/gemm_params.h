@@ -5,6 +5,10 @@
 
 namespace fp8g {
 
+// The operation a kernel instantiation computes.  kKindNTAcc: the plain GEMM
+// with an fp32 addend, D = bf16(C + A B^T scaled).
+enum Kind : int { kKindNT = 0, kKindContiguous = 1, kKindMasked = 2, kKindNTAcc = 3 };
+
 // Bits of the sticky device-side error word.
 enum : int { kErrTimeoutBit = 1, kErrBadGroupBit = 2 };
 

@@ -180,6 +180,27 @@ int fp8_gemm_sfa_ld(int M);
  */
 int fp8_gemm_set_override(int block_n, int split_ctas);
 
+/*
+ * CTA-pair kernel choice (process-wide):
+ *   mode  1 : run every unsplit plain, addend, contiguous and masked call on
+ *             CTA pairs -- clusters of two CTAs on neighbouring SMs that
+ *             share one 256 x 128 output tile through tcgen05.mma.cta_group::2
+ *             (each CTA loads its own 128 rows of A and half of the tile's B;
+ *             nothing is multicast) -- unless a block_n override other than
+ *             128 is set;
+ *   mode  0 : the automatic choice (the default);
+ *   mode -1 : never use CTA pairs.
+ * Results are the same to within fp32 rounding order (bit-identical on
+ * exactly representable inputs).  Returns FP8G_ERR_INVALID_ARG for other
+ * values.  The environment variable FP8G_PAIR_MODE ("-1", "0" or "1"), read
+ * when the library loads, sets the same value; this call replaces it.
+ * Source of the sharing: DeepGEMM fp8_gemm.cuh, tma_copy<kNumTMAMulticast>
+ * and the cluster launch of Gemm::run (the pages share one m-block's A across
+ * the CTAs of a cluster; here the pair shares its B and each CTA's partial
+ * stays in its own tensor memory).
+ */
+int fp8_gemm_set_pair_mode(int mode);
+
 /* Workspace bytes for an explicit split over `split_ctas` CTAs with tiles of
  * `block_n` columns (the size fp8_gemm_workspace_size reports for the
  * automatic choice). */

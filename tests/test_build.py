@@ -11,11 +11,13 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-KERNEL = os.path.join(ROOT, "fp8_block_scaled_persistent_gb300", "csrc", "gemm_kernel.cuh")
+CSRC = os.path.join(ROOT, "fp8_block_scaled_persistent_gb300", "csrc")
+KERNEL = os.path.join(CSRC, "gemm_kernel.cuh")
+PAIR_KERNEL = os.path.join(CSRC, "gemm_kernel_pair.cuh")
 
 
-def _const(name):
-    m = re.search(rf"constexpr int {name} = (\d+);", open(KERNEL).read())
+def _const(name, path=KERNEL):
+    m = re.search(rf"constexpr int {name} = (\d+);", open(path).read())
     assert m, name
     return int(m.group(1))
 
@@ -42,6 +44,18 @@ def test_register_reallocation_fits_the_launch_allocation(ptxas_report):
     assert threads == 384
     kernels = [n for n in ptxas_report if "fp8_gemm_kernel" in n]
     assert len(kernels) == 12       # plain and addend: 2 tile widths x split or not; grouped: 2 x 2
+    for name in kernels:
+        regs = ptxas_report[name][0]
+        assert regs == launch, f"{name}: launched with {regs} registers, expected {launch}"
+        assert 128 * ctl + 256 * epi <= threads * regs, name
+        assert ctl % 8 == 0 and epi % 8 == 0 and 24 <= ctl <= epi <= 256
+
+
+def test_pair_kernel_register_split_fits(ptxas_report):
+    threads, launch = _const("kNumThreads"), _const("kLaunchRegs")
+    ctl, epi = _const("kPairRegsCtl", PAIR_KERNEL), _const("kPairRegsEpi", PAIR_KERNEL)
+    kernels = [n for n in ptxas_report if "fp8_gemm_pair_kernel" in n]
+    assert len(kernels) == 4        # plain, addend, contiguous, masked
     for name in kernels:
         regs = ptxas_report[name][0]
         assert regs == launch, f"{name}: launched with {regs} registers, expected {launch}"
