@@ -349,15 +349,15 @@ bool make_maps(LaunchArgs &a, const void *A, const float *SFA, const void *B, co
 // pair_panel_cols() columns; the scale views are those of make_maps.
 bool make_pair_maps(LaunchArgs &a, const void *A, const float *SFA, const void *B, const float *SFB, void *D,
                     long long a_rows, long long b_rows, long long d_rows, long long sfa_rows, int sfa_ld,
-                    long long sfb_count, int N, int K)
+                    long long sfb_count, int N, int K, int block_n)
 {
     const int pc = fp8g::pair_panel_cols();
     std::memset(&a.tmap_a2, 0, sizeof(a.tmap_a2));
     std::memset(&a.tmap_b2, 0, sizeof(a.tmap_b2));
     return make_map(&a.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, a_rows, K, 128, 128,
                     CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_map(&a.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, b_rows, K, 128,
-                    (uint32_t)fp8g::pair_block_n() / 2, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(&a.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, b_rows, K, 128, (uint32_t)block_n / 2,
+                    CU_TENSOR_MAP_SWIZZLE_128B) &&
            make_map(&a.tmap_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, N, d_rows, (uint64_t)N * 2, pc, 32,
                     panel_swizzle(pc)) &&
            make_map(&a.tmap_sfa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SFA, sfa_ld, sfa_rows, (uint64_t)sfa_ld * 4,
@@ -366,15 +366,17 @@ bool make_pair_maps(LaunchArgs &a, const void *A, const float *SFA, const void *
                     CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+// The pair tile width: the block_n override when one is set, else 256.
+int pair_bn() { return g_override_bn.load() ? g_override_bn.load() : 256; }
+
 // Whether an unsplit launch runs on CTA pairs, and over how many pairs.
-// `pair_tiles` is the number of 256-row pair tiles the problem has.
+// `pair_tiles` is the number of 256 x pair_bn() pair tiles the problem has.
 bool want_pair(long long pair_tiles, const DeviceInfo &dev, int &pairs)
 {
     const int mode = g_override_pair.load();
-    const int obn = g_override_bn.load();
-    if (mode < 0 || (obn != 0 && obn != fp8g::pair_block_n()) || pair_tiles <= 0)
+    if (mode < 0 || pair_tiles <= 0)
         return false;
-    pairs = fp8g::max_active_pairs(dev.id);
+    pairs = fp8g::max_active_pairs(dev.id, pair_bn());
     if (pairs <= 0)
         return false;
     if (mode > 0)
@@ -386,18 +388,18 @@ bool want_pair(long long pair_tiles, const DeviceInfo &dev, int &pairs)
 int run_nt_pair(const void *A, const float *SFA, const void *B, const float *SFB, const float *C, void *D, int M,
                 int N, int K, int pairs, const DeviceInfo &dev, fp8g_stream_t stream)
 {
-    const int bn = fp8g::pair_block_n();
+    const int bn = pair_bn();
     LaunchArgs a;
     fill_common(a.p, M, N, K, 1, SFA, SFB, D, nullptr, bn, dev);
     a.p.c = C;
     a.p.num_m_blocks = ceil_div(M, 256);
     a.p.group_m = 8;
     a.p.num_tiles = a.p.num_m_blocks * a.p.num_n_blocks;
-    if (!make_pair_maps(a, A, SFA, B, SFB, D, M, N, M, a.p.kb, a.p.sfa_ld, (long long)a.p.nb * a.p.kb, N, K))
+    if (!make_pair_maps(a, A, SFA, B, SFB, D, M, N, M, a.p.kb, a.p.sfa_ld, (long long)a.p.nb * a.p.kb, N, K, bn))
         return FP8G_ERR_CUDA;
     a.grid = 2 * std::min(pairs, a.p.num_tiles);
     a.stream = reinterpret_cast<cudaStream_t>(stream);
-    return to_status(fp8g::launch_pair(C ? fp8g::kKindNTAcc : fp8g::kKindNT, a));
+    return to_status(fp8g::launch_pair(C ? fp8g::kKindNTAcc : fp8g::kKindNT, bn, a));
 }
 
 // The plain GEMM, with or without the fp32 addend C (validated by the caller).
@@ -415,7 +417,7 @@ int run_nt(const void *A, const float *SFA, const void *B, const float *SFB, con
     if (c.split_ctas && !aligned(workspace, 256))
         return FP8G_ERR_MISALIGNED;
     int pairs = 0;
-    if (!c.split_ctas && want_pair((long long)ceil_div(M, 256) * ceil_div(N, fp8g::pair_block_n()), dev, pairs))
+    if (!c.split_ctas && want_pair((long long)ceil_div(M, 256) * ceil_div(N, pair_bn()), dev, pairs))
         return run_nt_pair(A, SFA, B, SFB, C, D, M, N, K, pairs, dev, stream);
 
     LaunchArgs a;
@@ -498,19 +500,20 @@ int fp8_gemm_grouped_contiguous(const void *A, const float *SFA, const void *B, 
     if ((st = current_device_info(dev)) != FP8G_OK)
         return st;
     int pairs = 0;
-    if (want_pair((long long)ceil_div(M_total, 256) * ceil_div(N, fp8g::pair_block_n()), dev, pairs)) {
+    if (want_pair((long long)ceil_div(M_total, 256) * ceil_div(N, pair_bn()), dev, pairs)) {
+        const int bn = pair_bn();
         LaunchArgs a;
-        fill_common(a.p, M_total, N, K, G, SFA, SFB, D, m_indices, fp8g::pair_block_n(), dev);
+        fill_common(a.p, M_total, N, K, G, SFA, SFB, D, m_indices, bn, dev);
         a.p.num_m_blocks = ceil_div(M_total, 256);
         a.p.group_m = 8;
         const int pair_tiles = a.p.num_m_blocks * a.p.num_n_blocks;
         a.p.num_tiles = 2 * pair_tiles;     // two passes (see the pair scheduler)
         if (!make_pair_maps(a, A, SFA, B, SFB, D, M_total, (long long)G * N, M_total, a.p.kb, a.p.sfa_ld,
-                            (long long)G * a.p.nb * a.p.kb, N, K))
+                            (long long)G * a.p.nb * a.p.kb, N, K, bn))
             return FP8G_ERR_CUDA;
         a.grid = 2 * std::min(pairs, pair_tiles);
         a.stream = reinterpret_cast<cudaStream_t>(stream);
-        return to_status(fp8g::launch_pair(fp8g::kKindContiguous, a));
+        return to_status(fp8g::launch_pair(fp8g::kKindContiguous, bn, a));
     }
     const int mb = M_total / 128;
     const int block_n = pick_block_n(N, (long long)mb * ceil_div(N, 256) >= dev.sms);
@@ -548,18 +551,19 @@ int fp8_gemm_grouped_masked(const void *A, const float *SFA, const void *B, cons
     if ((st = current_device_info(dev)) != FP8G_OK)
         return st;
     int pairs = 0;
-    if (want_pair((long long)G * ceil_div(M_max, 256) * ceil_div(N, fp8g::pair_block_n()), dev, pairs)) {
+    if (want_pair((long long)G * ceil_div(M_max, 256) * ceil_div(N, pair_bn()), dev, pairs)) {
+        const int bn = pair_bn();
         LaunchArgs a;
-        fill_common(a.p, M_max, N, K, G, SFA, SFB, D, masked_m, fp8g::pair_block_n(), dev);
+        fill_common(a.p, M_max, N, K, G, SFA, SFB, D, masked_m, bn, dev);
         a.p.num_m_blocks = ceil_div(M_max, 256);
         a.p.group_m = a.p.num_m_blocks;
         const long long tiles_max = (long long)G * a.p.num_m_blocks * a.p.num_n_blocks;
         if (!make_pair_maps(a, A, SFA, B, SFB, D, (long long)G * M_max, (long long)G * N, (long long)G * M_max,
-                            (long long)G * a.p.kb, a.p.sfa_ld, (long long)G * a.p.nb * a.p.kb, N, K))
+                            (long long)G * a.p.kb, a.p.sfa_ld, (long long)G * a.p.nb * a.p.kb, N, K, bn))
             return FP8G_ERR_CUDA;
         a.grid = 2 * (int)std::min<long long>(pairs, tiles_max);
         a.stream = reinterpret_cast<cudaStream_t>(stream);
-        return to_status(fp8g::launch_pair(fp8g::kKindMasked, a));
+        return to_status(fp8g::launch_pair(fp8g::kKindMasked, bn, a));
     }
     const int mb = ceil_div(M_max, 128);
     const long long tiles_max256 = (long long)G * mb * ceil_div(N, 256);
@@ -735,7 +739,7 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const float *SFA, const void *
             return st;
     }
     int pairs = 0;
-    if (!c.split_ctas && want_pair((long long)ceil_div(M, 256) * ceil_div(N, fp8g::pair_block_n()), dev, pairs))
+    if (!c.split_ctas && want_pair((long long)ceil_div(M, 256) * ceil_div(N, pair_bn()), dev, pairs))
         return run_nt_pair(A, SFA, B, SFB, nullptr, D, M, N, K, pairs, dev, stream);
     const size_t counters = ((size_t)c.tiles * 8 * sizeof(int) + 255) / 256 * 256;
 

@@ -1,5 +1,6 @@
 // gemm_kernel_pair.cuh -- the CTA-pair variant of the FP8 block-scaled GEMM:
-// one 256 x 128 output tile per cluster of two CTAs on neighbouring SMs.
+// one 256 x BN output tile (BN = 128 or 256) per cluster of two CTAs on
+// neighbouring SMs.
 //
 // What is computed is the same as in gemm_kernel.cuh (DeepGEMM fp8_gemm.cuh,
 // fp8_gemm_kernel: each 128-wide K block's partial promoted with
@@ -9,16 +10,14 @@
 // multicast):
 //
 //   * rank 0 of the cluster (the leader) issues tcgen05.mma.cta_group::2 with
-//     M = 256, N = 128: each CTA holds its own 128 rows of A and its own 64
+//     M = 256, N = BN: each CTA holds its own 128 rows of A and its own BN/2
 //     rows (half) of B in its shared memory, and each CTA's tensor memory
-//     receives its 128 rows x 128 columns of the partial.  Each SM so loads
-//     24 KB per K block for a 128 x 128 share of the output: the B traffic of
-//     a 128 x 256 tile at the shared-memory cost of a 128 x 128 one;
-//   * with 128 columns per partial, the 512 tensor-memory columns hold FOUR
-//     partial buffers per CTA, so the MMA of K block k + 4 waits for the
-//     epilogue to have read block k: three K blocks of slack for the
-//     "MMA completes -> epilogue reads -> buffer freed" round trip, where a
-//     128 x 256 tile on one SM has one;
+//     receives its 128 rows x BN columns of the partial.  At BN = 256 each
+//     SM loads 32 KB per K block for a 128 x 256 share of the output, where a
+//     128 x 256 tile on one SM loads 48 KB;
+//   * at BN = 128 the 512 tensor-memory columns hold four partial buffers per
+//     CTA (three K blocks of slack for the "MMA completes -> epilogue reads
+//     -> buffer freed" round trip), at BN = 256 two;
 //   * both producers load into their own CTA but signal the leader's
 //     full barrier (cp.async.bulk.tensor .cta_group::2, each producer adding
 //     its own bytes with a remote arrive.expect_tx); the leader's one commit
@@ -42,24 +41,24 @@
 
 namespace fp8g {
 
-// Registers per thread after reallocation in the pair kernel: the epilogue
-// holds 64 accumulator columns (not 128), so the control warpgroup keeps more.
-// The launch allocation is 384 x 168 = 64512; 128 x 72 + 256 x 208 = 62464.
-constexpr int kPairRegsCtl = 72;
-constexpr int kPairRegsEpi = 208;
-static_assert(128 * kPairRegsCtl + 256 * kPairRegsEpi <= kNumThreads * kLaunchRegs,
-              "register reallocation exceeds the launch allocation");
-
+// Pair tiles are 256 x BN: each CTA holds 128 rows of A and BN/2 rows of B
+// per K block, and receives a 128 x BN partial in its tensor memory.
+//   BN = 128: four partial buffers per CTA (the round trip has three K
+//             blocks of slack) and 24 KB of operands per SM per K block, but
+//             only 256 tensor cycles per K block for the one issuing thread;
+//   BN = 256: two partial buffers, 512 tensor cycles per K block, and 32 KB
+//             of operands per SM per K block where a 128 x 256 tile on one SM
+//             loads 48 KB.
 template <int BN>
 struct PairCfg {
-    static_assert(BN == 128, "pair tiles are 256 x 128");
+    static_assert(BN == 128 || BN == 256, "pair tiles are 256 x 128 or 256 x 256");
     static constexpr int kPairRows = 2 * kBM;          // output rows per pair tile
     static constexpr int kBHalfRows = BN / 2;          // B rows each CTA loads
-    static constexpr int kStages = 7;                  // A/B operand ring
-    static constexpr int kAccBufs = kTmemCols / BN;    // 4 partial buffers per CTA
+    static constexpr int kStages = BN == 128 ? 7 : 4;  // A/B operand ring
+    static constexpr int kAccBufs = kTmemCols / BN;    // partial buffers per CTA
     static constexpr int kScaleSlots = 4;
     static constexpr int kABytes = kBM * kBK;          // 16 KB
-    static constexpr int kBBytes = kBHalfRows * kBK;   // 8 KB
+    static constexpr int kBBytes = kBHalfRows * kBK;   // 8 or 16 KB
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kSfbRows = BN / 128;
     static constexpr int kSlotSfaBytes = kScaleChunk * kBM * 4;
@@ -74,14 +73,45 @@ struct PairCfg {
     static constexpr int kBarriers = 2 * kStages + kAccBufs + 2 * kScaleSlots + 1;
     static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + kScaleSlots * kSlotBytes +
                                       kBarriers * 8 + 16 + 1024 /* alignment slack */;
+    // registers per thread after reallocation: the epilogue holds BN/2
+    // accumulator columns; the launch allocation is 384 x 168 = 64512
+    static constexpr int kRegsCtl = BN == 128 ? 72 : 40;
+    static constexpr int kRegsEpi = BN == 128 ? 208 : 232;
+    static_assert(128 * kRegsCtl + 256 * kRegsEpi <= kNumThreads * kLaunchRegs,
+                  "register reallocation exceeds the launch allocation");
     static_assert(kSlotTxBytes <= kSlotBytes, "scale slot");
     static_assert(kSlotBytes % 128 == 0 && kSlotSfaBytes % 128 == 0 && kStagingBytes % 1024 == 0 &&
                       kABytes % 1024 == 0 && kBBytes % 1024 == 0 && kPanelBytes % 1024 == 0,
                   "TMA destinations and sources must stay 128-byte (swizzled: 1024-byte) aligned");
-    static_assert(kPanelsPerWarp == 1, "one staging panel per warp");
     static_assert(kStages >= kAccBufs, "the epilogue's wait on a stage's MMA completion must not alias");
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
+
+// The same K-block promotion as promote_block, releasing the buffer on the
+// leader's barrier (a shared::cluster address) once its last load landed.
+template <int COLS, int LD>
+__device__ __forceinline__ void promote_block_pair(float (&acc)[COLS], uint32_t taddr, const float *pa,
+                                                   const float *pb, uint32_t tempty_cluster_addr, int lane)
+{
+    constexpr int NCH = COLS / LD;
+    static_assert(COLS % LD == 0, "column split");
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+        uint32_t v[LD];
+        tmem_ld(taddr + c * LD, v);
+        if (c == 0)
+            s = *pa * *pb;
+        tmem_wait_ld(v);
+        if (c + 1 == NCH) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_cluster(tempty_cluster_addr);
+        }
+        fma_cols<LD>(acc + c * LD, v, s);
+    }
+}
 
 // Work unit of one CTA of a pair: its 128 rows of a 256-row pair tile.
 struct PairWork {
@@ -108,16 +138,18 @@ struct PairWork {
 template <int KIND>
 struct PairScheduler {
     const Params &p;
-    int rank, npairs, next_tile;
+    int next_tile;
     int walk_g = 0, walk_base = 0, walk_tiles = -1, walk_count = 0;
     bool report;
 
-    __device__ PairScheduler(const Params &pp, int r, bool report_bad_groups)
-        : p(pp), rank(r), report(report_bad_groups)
+    __device__ PairScheduler(const Params &pp, bool report_bad_groups) : p(pp), report(report_bad_groups)
     {
-        npairs = (int)gridDim.x / 2;
         next_tile = (int)blockIdx.x / 2;
     }
+
+    // (read from special registers when needed rather than held)
+    __device__ __forceinline__ int npairs() const { return (int)gridDim.x / 2; }
+    __device__ __forceinline__ int rank() const { return (int)cluster_ctarank(); }
 
     __device__ __forceinline__ bool group_ok(int g) const { return g >= 0 && g < p.G; }
 
@@ -127,11 +159,11 @@ struct PairScheduler {
             if (next_tile >= p.num_tiles)
                 return false;
             const int t = next_tile;
-            next_tile += npairs;
+            next_tile += npairs();
             raster(t, p.num_m_blocks, p.num_n_blocks, p.group_m, w.m_blk, w.n_blk);
             w.g = 0;
             w.tile = t;
-            w.a_row0 = w.m_blk * (2 * kBM) + kBM * rank;
+            w.a_row0 = w.m_blk * (2 * kBM) + kBM * rank();
             w.sfa_x = w.a_row0;
             w.valid_rows = min(max(p.rows - w.a_row0, 0), kBM);
             return true;
@@ -139,7 +171,7 @@ struct PairScheduler {
             const int T = p.num_tiles / 2;     // pair tiles of one pass
             while (next_tile < p.num_tiles) {
                 const int t = next_tile;
-                next_tile += npairs;
+                next_tile += npairs();
                 const bool pass1 = t >= T;
                 raster(pass1 ? t - T : t, p.num_m_blocks, p.num_n_blocks, p.group_m, w.m_blk, w.n_blk);
                 const int r0 = w.m_blk * (2 * kBM);
@@ -169,9 +201,9 @@ struct PairScheduler {
                     live1 = true;
                 }
                 w.tile = t;
-                w.a_row0 = r0 + kBM * rank;
+                w.a_row0 = r0 + kBM * rank();
                 w.sfa_x = w.a_row0;
-                w.valid_rows = (rank ? live1 : live0) ? kBM : 0;
+                w.valid_rows = (rank() ? live1 : live0) ? kBM : 0;
                 return true;
             }
             return false;
@@ -190,12 +222,12 @@ struct PairScheduler {
                 walk_tiles = -1;
                 ++walk_g;
             }
-            next_tile += npairs;
+            next_tile += npairs();
             const int mb = (walk_count + 2 * kBM - 1) / (2 * kBM);
             raster(t - walk_base, mb, p.num_n_blocks, mb, w.m_blk, w.n_blk);
             w.g = walk_g;
             w.tile = t;
-            const int row_in_group = w.m_blk * (2 * kBM) + kBM * rank;
+            const int row_in_group = w.m_blk * (2 * kBM) + kBM * rank();
             w.a_row0 = walk_g * p.rows + row_in_group;
             w.sfa_x = row_in_group;
             w.valid_rows = min(max(walk_count - row_in_group, 0), kBM);
@@ -283,10 +315,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const WaitCtl ctl{abort_flag, p.error_word, p.timeout_ns, peer_abort};
 
     if (warp < kEpiWarp0) {
-        regs_dealloc<kPairRegsCtl>();
+        regs_dealloc<C::kRegsCtl>();
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------ TMA producer (both CTAs)
-            PairScheduler<KIND> sched(p, rank, false);
+            PairScheduler<KIND> sched(p, false);
             PairWork w;
             Ring ring, sring;
             const uint32_t leader_full = mapa_shared(smem_u32(full), 0);
@@ -339,7 +371,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     mbar_wait_drain(&sfull[i], (sissued_parity >> i) & 1u, p.timeout_ns);
         } else if (warp == 1 && lane == 0 && rank == 0) {
             // ------------------------------------------------ MMA issuer (leader)
-            PairScheduler<KIND> sched(p, rank, false);
+            PairScheduler<KIND> sched(p, false);
             PairWork w;
             Ring ring, acc;
             constexpr uint32_t idesc = idesc_e4m3_f32(2 * kBM, BN);
@@ -370,13 +402,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_wait_drain(drain, 0, p.timeout_ns);
         }
     } else {
-        regs_alloc<kPairRegsEpi>();
+        regs_alloc<C::kRegsEpi>();
         // ------------------------------------------------ epilogue warps (both CTAs)
         const int ew = warp - kEpiWarp0;     // 0..7
         const int q = warp & 3;              // TMEM lane quarter this warp may access
         const int h = ew >> 2;               // column half of the tile
         const int row_in_tile = 32 * q + lane;
-        uint8_t *panel = sm_stage_d + ew * C::kPanelBytes;
+        const int sfb_row = (BN == 256) ? h : 0;   // the warp's 128-column block of the tile
+        uint8_t *panels = sm_stage_d + ew * C::kPanelsPerWarp * C::kPanelBytes;
         const uint32_t leader_tempty = mapa_shared(smem_u32(tempty), 0);
 
         if (KIND == kKindMasked && blockIdx.x == 0 && ew == 0) {
@@ -387,7 +420,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
         }
 
-        PairScheduler<KIND> sched(p, rank, rank == 0 && ew == 0 && lane == 0);
+        PairScheduler<KIND> sched(p, rank == 0 && ew == 0 && lane == 0);
         PairWork w;
         Ring ring, acc_ring, sring;
         bool ok = true;
@@ -424,22 +457,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 tc_fence_after_sync();
                 const uint8_t *slot = sm_scales + sring.i * C::kSlotBytes;
                 const float *pa = reinterpret_cast<const float *>(slot) + kc * kBM + row_in_tile;
-                const int sfb_idx0 = (w.g * p.nb + (w.n_blk * BN) / 128) * p.kb + (k - kc);
-                const float *pb = reinterpret_cast<const float *>(slot + C::kSlotSfaBytes) + (sfb_idx0 & 3) + kc;
+                const int sfb_idx0 = (w.g * p.nb + (w.n_blk * BN) / 128 + sfb_row) * p.kb + (k - kc);
+                const float *pb = reinterpret_cast<const float *>(slot + C::kSlotSfaBytes +
+                                                                  C::kSlotSfbStride * sfb_row) + (sfb_idx0 & 3) + kc;
 
+                // promote, and hand the buffer back to the leader's MMA issuer
                 const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + acc_ring.i * BN + h * COLS;
-                {
-                    uint32_t v[COLS];
-                    tmem_ld(taddr, v);
-                    const float s = *pa * *pb;
-                    tmem_wait_ld(v);
-                    // hand the buffer back to the leader's MMA issuer
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive_cluster(leader_tempty + 8u * acc_ring.i);
-                    fma_cols<COLS>(acc, v, s);
-                }
+                promote_block_pair<COLS, 64>(acc, taddr, pa, pb, leader_tempty + 8u * acc_ring.i, lane);
                 acc_ring.template next<NACC>();
                 ring.template next<S>();
                 if (kc == kScaleChunk - 1 || k + 1 == p.kb) {
@@ -461,8 +485,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (lane == 0)
                 bulk_wait_group_read<0>();
             __syncwarp();
-            if (x < p.N && rows_ok > 0)
-                store_panel<C::kPanelCols, false>(acc, panel, &tmap_d, p, x, y_row0, rows_ok, lane);
+            constexpr int PC = C::kPanelCols;
+#pragma unroll
+            for (int pi = 0; pi < COLS / PC; ++pi)
+                if (x + pi * PC < p.N && rows_ok > 0)
+                    store_panel<PC, false>(acc + pi * PC, panels + pi * C::kPanelBytes, &tmap_d, p, x + pi * PC,
+                                           y_row0, rows_ok, lane);
         }
         if constexpr (KIND == kKindNTAcc)
             cp_async_wait_all();

@@ -32,14 +32,14 @@ cudaError_t launch_nt_acc(int block_n, bool split, const LaunchArgs &a);   // a.
 cudaError_t launch_contiguous(int block_n, const LaunchArgs &a);
 cudaError_t launch_masked(int block_n, const LaunchArgs &a);
 
-// The CTA-pair kernel (gemm_pair.cu): clusters of two CTAs, one tile of 256
-// rows x pair_block_n() columns per pair.  `kind` is a Kind; a.grid is twice
-// the number of pairs; the tensor maps are those of make_pair_maps in api.cu
-// (B boxes of pair_block_n()/2 rows, D panels of pair_panel_cols() columns).
-cudaError_t launch_pair(int kind, const LaunchArgs &a);
-int pair_block_n();
+// The CTA-pair kernel (gemm_pair.cu, gemm_pair256.cu): clusters of two CTAs,
+// one tile of 256 rows x block_n (128 or 256) columns per pair.  `kind` is a
+// Kind; a.grid is twice the number of pairs; the tensor maps are those of
+// make_pair_maps in api.cu (B boxes of block_n/2 rows, D panels of
+// pair_panel_cols() columns).
+cudaError_t launch_pair(int kind, int block_n, const LaunchArgs &a);
 int pair_panel_cols();
 // Clusters of two that can be resident at once on device `dev` (0 on failure).
-int max_active_pairs(int dev);
+int max_active_pairs(int dev, int block_n);
 
 }  // namespace fp8g

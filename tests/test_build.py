@@ -53,14 +53,19 @@ def test_register_reallocation_fits_the_launch_allocation(ptxas_report):
 
 def test_pair_kernel_register_split_fits(ptxas_report):
     threads, launch = _const("kNumThreads"), _const("kLaunchRegs")
-    ctl, epi = _const("kPairRegsCtl", PAIR_KERNEL), _const("kPairRegsEpi", PAIR_KERNEL)
+    text = open(PAIR_KERNEL).read()
+    ctl = re.search(r"kRegsCtl = BN == 128 \? (\d+) : (\d+);", text)
+    epi = re.search(r"kRegsEpi = BN == 128 \? (\d+) : (\d+);", text)
+    assert ctl and epi
     kernels = [n for n in ptxas_report if "fp8_gemm_pair_kernel" in n]
-    assert len(kernels) == 4        # plain, addend, contiguous, masked
+    assert len(kernels) == 8        # 2 tile widths x plain, addend, contiguous, masked
     for name in kernels:
         regs = ptxas_report[name][0]
         assert regs == launch, f"{name}: launched with {regs} registers, expected {launch}"
-        assert 128 * ctl + 256 * epi <= threads * regs, name
-        assert ctl % 8 == 0 and epi % 8 == 0 and 24 <= ctl <= epi <= 256
+        i = 0 if "ILi128E" in name else 1
+        c, e = int(ctl.group(1 + i)), int(epi.group(1 + i))
+        assert 128 * c + 256 * e <= threads * regs, name
+        assert c % 8 == 0 and e % 8 == 0 and 24 <= c <= e <= 256
 
 
 def test_kernels_do_not_spill(ptxas_report):

@@ -2,7 +2,7 @@
 tiles through tcgen05.mma.cta_group::2) with the CPU oracle, through the C
 ABI with fp8_gemm_set_pair_mode(1).
 
-Covers the plain GEMM on ragged shapes (pair tiles whose second CTA has few
+Every test runs with both pair tile widths.  Covers the plain GEMM on ragged shapes (pair tiles whose second CTA has few
 or no rows, column tails), exact small-integer inputs bit for bit, the
 contiguous layout with pair tiles whose two 128-row blocks belong to
 different groups (the second pass), skipped and out-of-range blocks, the
@@ -23,13 +23,16 @@ pytestmark = pytest.mark.gpu
 THREADS = oracle.default_threads()
 
 
-@pytest.fixture(autouse=True)
-def _pair_mode():
+@pytest.fixture(autouse=True, params=[128, 256], ids=["pair256x128", "pair256x256"])
+def pair_bn(request):
+    """Every test runs with both pair tile widths (256 x 128 and 256 x 256);
+    splitting K is forbidden so that the pair kernel is what runs."""
     import fp8_block_scaled_persistent_gb300 as fg
-    fg.fp8_gemm_set_override(0, 0)
+    assert fg.fp8_gemm_set_override(request.param, -1) == fg.FP8G_OK
     assert fg.fp8_gemm_set_pair_mode(1) == fg.FP8G_OK
-    yield
+    yield request.param
     fg.fp8_gemm_set_pair_mode(0)
+    fg.fp8_gemm_set_override(0, 0)
     assert fg.fp8_gemm_get_device_error() == 0
 
 
