@@ -58,7 +58,9 @@ DEFAULT_PAIR = ["dense_4096x7168x2048", "dense_4096x24576x1536"]
 # lines list them
 ALL_SHAPES = ["single_128x256x512", "dense_4096x7168x2048", "dense_4096x24576x1536",
               "smallm_64x7168x16384", "smallm_128x7168x16384",
-              "contiguous_g8_n4096_k7168", "masked_g16_m256_n7168_k2048"]
+              "contiguous_g8_n4096_k7168", "masked_g16_m256_n7168_k2048",
+              # the power-of-two (UE8M0) scale variant on the dense shapes
+              "ue8m0_4096x7168x2048", "ue8m0_4096x24576x1536"]
 FP8_OVER_BF16 = 2.0      # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 FP8_NOMINAL_TFLOPS = 4500.0   # GB300 nominal dense FP8 (no sparsity)
 HBM_BOUND = {"smallm_64x7168x16384", "smallm_128x7168x16384", "masked_g16_m256_n7168_k2048"}
@@ -632,6 +634,9 @@ def shape_parity(case, threads):
             elif p.kind == "contiguous":
                 ref = oracle.gemm_grouped_contiguous_rows(p.A, p.SFA, p.B, p.SFB, p.m_indices, p.M, p.N, p.K,
                                                           p.G, rows, threads=threads)
+                got = d[rows]
+            elif p.kind == "nt_ue8m0":
+                ref = oracle.gemm_nt_ue8m0_rows(p.A, p.SFA, p.B, p.SFB, p.M, p.N, p.K, rows, threads=threads)
                 got = d[rows]
             elif p.kind == "nt_acc":
                 ref = oracle.gemm_nt_acc_rows(p.A, p.SFA, p.B, p.SFB, p.C, p.M, p.N, p.K, rows,

@@ -33,7 +33,8 @@ FP8G_KIND_GROUPED_MASKED = 2
 
 # every symbol the header declares, in declaration order
 EXPORTS = (
-    "fp8_gemm_nt", "fp8_gemm_nt_accumulate", "fp8_gemm_grouped_contiguous", "fp8_gemm_grouped_masked",
+    "fp8_gemm_nt", "fp8_gemm_nt_accumulate", "fp8_gemm_nt_ue8m0", "fp8_gemm_grouped_contiguous",
+    "fp8_gemm_grouped_masked",
     "fp8_gemm_workspace_size", "fp8_gemm_get_device_error", "fp8_gemm_status_string",
     "fp8_gemm_sfa_ld", "fp8_gemm_set_override", "fp8_gemm_set_pair_mode", "fp8_gemm_workspace_size_for",
     "fp8_gemm_set_wait_timeout_ns", "fp8_gemm_nt_noalloc", "fp8_gemm_version",
@@ -63,6 +64,8 @@ def library(path: str = LIB_PATH):
         lib.fp8_gemm_nt.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp, sz, vp]
         lib.fp8_gemm_nt_accumulate.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, vp, sz, vp]
         lib.fp8_gemm_nt_accumulate.restype = i
+        lib.fp8_gemm_nt_ue8m0.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
+        lib.fp8_gemm_nt_ue8m0.restype = i
         lib.fp8_gemm_grouped_contiguous.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, vp, sz, vp]
         lib.fp8_gemm_grouped_masked.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, vp, sz, vp]
         for f in ("fp8_gemm_nt", "fp8_gemm_grouped_contiguous", "fp8_gemm_grouped_masked"):
@@ -130,6 +133,14 @@ def fp8_gemm_nt_accumulate(A, SFA, B, SFB, C, D, M, N, K, workspace=None, stream
     wp, wb = _ws(workspace)
     return library().fp8_gemm_nt_accumulate(_ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(C), _ptr(D),
                                              int(M), int(N), int(K), wp, wb, _stream(stream))
+
+
+def fp8_gemm_nt_ue8m0(A, SFA_e, B, SFB_e, D, M, N, K, stream=None) -> int:
+    """D[M][N] (bf16) = A x B^T with power-of-two scales given as UE8M0 bytes:
+    SFA_e uint8 [K/128][sfa_ld(M)], SFB_e uint8 [ceil(N/128)][K/128].
+    Returns the status code."""
+    return library().fp8_gemm_nt_ue8m0(_ptr(A), _ptr(SFA_e), _ptr(B), _ptr(SFB_e), _ptr(D),
+                                       int(M), int(N), int(K), _stream(stream))
 
 
 def fp8_gemm_grouped_contiguous(A, SFA, B, SFB, D, m_indices, M_total, N, K, G,

@@ -581,6 +581,46 @@ int fp8_gemm_grouped_masked(const void *A, const float *SFA, const void *B, cons
     return to_status(fp8g::launch_masked(block_n, a));
 }
 
+int fp8_gemm_nt_ue8m0(const void *A, const void *SFA_e, const void *B, const void *SFB_e, void *D, int M, int N,
+                      int K, fp8g_stream_t stream)
+{
+    if (!A || !SFA_e || !B || !SFB_e || !D)
+        return FP8G_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K <= 0)
+        return FP8G_ERR_INVALID_ARG;
+    if (K % 128 != 0 || N % 16 != 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return FP8G_ERR_UNSUPPORTED;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16))
+        return FP8G_ERR_MISALIGNED;
+    if (M == 0 || N == 0)
+        return FP8G_OK;
+    DeviceInfo dev;
+    int st;
+    if ((st = current_device_info(dev)) != FP8G_OK)
+        return st;
+    const int bn = fp8g::ue8m0_block_n();
+    LaunchArgs a;
+    fill_common(a.p, M, N, K, 1, nullptr, nullptr, D, nullptr, bn, dev);
+    a.p.sfa_e = static_cast<const uint8_t *>(SFA_e);
+    a.p.sfb_e = static_cast<const uint8_t *>(SFB_e);
+    a.p.num_m_blocks = ceil_div(M, 128);
+    a.p.group_m = 8;
+    a.p.num_tiles = a.p.num_m_blocks * a.p.num_n_blocks;
+    const int pc = fp8g::ue8m0_panel_cols();
+    std::memset(&a.tmap_sfa, 0, sizeof(a.tmap_sfa));
+    std::memset(&a.tmap_sfb, 0, sizeof(a.tmap_sfb));
+    std::memset(&a.tmap_a2, 0, sizeof(a.tmap_a2));
+    std::memset(&a.tmap_b2, 0, sizeof(a.tmap_b2));
+    if (!make_map(&a.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&a.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, (uint32_t)bn,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&a.tmap_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, N, M, (uint64_t)N * 2, pc, 32, panel_swizzle(pc)))
+        return FP8G_ERR_CUDA;
+    a.grid = std::min(dev.sms, a.p.num_tiles);
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    return to_status(fp8g::launch_ue8m0(a));
+}
+
 size_t fp8_gemm_workspace_size(int kind, int M, int N, int K, int G)
 {
     (void)G;

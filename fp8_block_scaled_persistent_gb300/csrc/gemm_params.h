@@ -1,6 +1,7 @@
 // gemm_params.h -- the kernel's by-value argument block (host and device).
 #pragma once
 
+#include <cstdint>
 #include <cuda_bf16.h>
 
 namespace fp8g {
@@ -25,6 +26,8 @@ struct Params {
     int sfa_ld;        // round_up(rows, 4)
     const float *sfa;
     const float *sfb;
+    const uint8_t *sfa_e;  // power-of-two scales: UE8M0 bytes, layouts of sfa and sfb
+    const uint8_t *sfb_e;
     const int *layout; // contiguous: m_indices; masked: masked_m
     __nv_bfloat16 *d;
     const float *c;    // NT with an addend: fp32 [rows][N], read-only, not overlapping d

@@ -42,4 +42,12 @@ int pair_panel_cols();
 // Clusters of two that can be resident at once on device `dev` (0 on failure).
 int max_active_pairs(int dev, int block_n);
 
+// The power-of-two-scale kernel (gemm_ue8m0.cu): tiles of 128 x
+// ue8m0_block_n(), a.p.sfa_e / a.p.sfb_e set; tensor maps tmap_a (boxes of
+// 128 rows), tmap_b (boxes of ue8m0_block_n() rows), tmap_d (panels of
+// ue8m0_panel_cols() columns).
+cudaError_t launch_ue8m0(const LaunchArgs &a);
+int ue8m0_block_n();
+int ue8m0_panel_cols();
+
 }  // namespace fp8g

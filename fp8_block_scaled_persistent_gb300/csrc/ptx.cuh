@@ -535,6 +535,59 @@ __device__ __forceinline__ void st_cg_f4(float4 *p, float4 v)
                  : "memory");
 }
 
+// ---------------------------------------------------------------- block-scaled MMA (power-of-two scales)
+
+// D(tmem) (+)= (A * 2^(sa-127)) (B * 2^(sb-127))^T, E4M3 x E4M3 -> F32,
+// M x N x 32, with one UE8M0 scale byte per row of A and per column of B
+// read from tensor memory (scale_vec::1X: one scale per 32 K elements).
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: A = B = E4M3,
+// both K-major, D = F32 (implied), UE8M0 scales, scale byte 0 of each
+// tensor-memory word (scale-factor ids 0), shape M x N (x 32).
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(uint32_t M, uint32_t N)
+{
+    return (0u << 4)              // scale-factor id of B
+           | (0u << 7)            // A format E4M3
+           | (0u << 10)           // B format E4M3
+           | (0u << 15)           // A K-major
+           | (0u << 16)           // B K-major
+           | ((N >> 3) << 17)     // N / 8
+           | (1u << 23)           // scale format UE8M0
+           | ((M >> 4) << 24)     // M / 16
+           | (0u << 29);          // scale-factor id of A
+}
+
+// 32 lanes x 4 / 8 consecutive 32-bit columns from registers: thread t of the
+// warp writes lane (taddr.lane + t).
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                                  uint32_t e, uint32_t f, uint32_t g, uint32_t h)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
+                 : "memory");
+}
+
+// Waits for this thread's outstanding tcgen05.st.
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // ---------------------------------------------------------------- CTA pairs (cta_group::2)
 //
 // A cluster of two CTAs on neighbouring SMs shares one MMA: rank 0 (the

@@ -110,6 +110,29 @@ int fp8_gemm_nt_accumulate(const void *A, const float *SFA, const void *B, const
                            void *workspace, size_t workspace_bytes, fp8g_stream_t stream);
 
 /*
+ * Plain GEMM with power-of-two (UE8M0) scales:
+ *   D[m][n] = bf16( sum_k 2^(SFA_e[k][m] - 127) * 2^(SFB_e[n/128][k] - 127) *
+ *                   sum_{t < 128} A[m][128k+t] * B[n][128k+t] )
+ * The method's granularity is kept (one scale per row of A per 128-wide K
+ * block, one per 128 x 128 block of B); each scale is a UE8M0 byte e of the
+ * OCP MX formats, value 2^(e - 127) (0xFF is not a valid scale).  The tensor
+ * cores' block-scaled MMA applies the scales, so the fp32 sum over all of K
+ * stays in tensor memory: the product of two power-of-two scales and an
+ * E4M3 product is exact, and the only roundings are the fp32 accumulation
+ * and the final bf16.
+ * Layouts (device pointers): A e4m3 [M][K], B e4m3 [N][K], D bf16 [M][N] as
+ * for fp8_gemm_nt; SFA_e uint8 [K/128][fp8_gemm_sfa_ld(M)] (M-major, pad
+ * entries never read), SFB_e uint8 [ceil(N/128)][K/128].  SFA_e and SFB_e
+ * need no alignment; A, B and D 16 bytes.  K % 128 == 0, N % 16 == 0.
+ * No workspace; M == 0 or N == 0 is a no-op.  Errors as for fp8_gemm_nt.
+ * Source: TCGen05 Copy Instruction (Triton Gluon tutorial), the closing
+ * section on block-scaled MMA (scales held in tensor memory beside the
+ * accumulator), applied to the scaling of DeepGEMM fp8_gemm.cuh.
+ */
+int fp8_gemm_nt_ue8m0(const void *A, const void *SFA_e, const void *B, const void *SFB_e,
+                      void *D, int M, int N, int K, fp8g_stream_t stream);
+
+/*
  * Grouped GEMM, contiguous layout (MoE experts): rows of A are concatenated
  * over groups; m_indices[r] (device int32 [M_total]) names the group of row
  * r, and row r is multiplied by B[m_indices[r]].  Every 128-row block must

@@ -36,6 +36,8 @@ def call(p, t, D, workspace=None, stream=None, layout=None) -> int:
     if p.kind == "nt":
         return fg.fp8_gemm_nt(t["A"], t["SFA"], t["B"], t["SFB"], D, p.M, p.N, p.K,
                               workspace=workspace, stream=stream)
+    if p.kind == "nt_ue8m0":
+        return fg.fp8_gemm_nt_ue8m0(t["A"], t["SFA"], t["B"], t["SFB"], D, p.M, p.N, p.K, stream=stream)
     if p.kind == "nt_acc":
         return fg.fp8_gemm_nt_accumulate(t["A"], t["SFA"], t["B"], t["SFB"], t["C"], D, p.M, p.N, p.K,
                                          workspace=workspace, stream=stream)
@@ -57,6 +59,8 @@ def workspace_for(p, device="cuda"):
     """A zero-filled workspace of the size the library asks for (None if 0)."""
     import torch
     import fp8_block_scaled_persistent_gb300 as fg
+    if p.kind == "nt_ue8m0":
+        return None
     kind = {"nt": 0, "nt_acc": 0, "contiguous": 1, "masked": 2}[p.kind]
     n = fg.fp8_gemm_workspace_size(kind, p.M, p.N, p.K, p.G)
     if n == 0:

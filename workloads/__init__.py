@@ -392,6 +392,9 @@ WORKLOADS = {
         masked_counts(16, 256, seed=seed), 256, 7168, 2048, seed, "masked_g16_m256_n7168_k2048"),
     # the accumulate variant (D = bf16(C + A B^T)) on the first dense shape
     "acc_4096x7168x2048": lambda seed=0: make_nt_acc(4096, 7168, 2048, seed, "acc_4096x7168x2048"),
+    # power-of-two (UE8M0) scales on the dense shapes
+    "ue8m0_4096x7168x2048": lambda seed=0: make_nt_ue8m0(4096, 7168, 2048, seed, "ue8m0_4096x7168x2048"),
+    "ue8m0_4096x24576x1536": lambda seed=0: make_nt_ue8m0(4096, 24576, 1536, seed, "ue8m0_4096x24576x1536"),
 }
 
 
