@@ -18,7 +18,7 @@
 //
 // One CTA per SM, 512 threads, tiles of 128 x 256:
 //   warp 0      TMA producer: A 128 x 128 and B 256 x 128 e4m3 tiles,
-//               128-byte swizzled, into a 3-stage ring.
+//               128-byte swizzled, into a 4-stage ring.
 //   warp 1      MMA issuer: per K block 4 x (128 x 256 x 32) block-scaled
 //               MMAs accumulating into tensor-memory columns 0 .. 255; one
 //               commit per K block frees the operand stage; one commit at
@@ -26,8 +26,9 @@
 //   warps 4-11  epilogue: at the end of a tile, each reads its 32 rows x
 //               128 columns of the accumulator (two tcgen05.ld), releases it
 //               for the next tile, converts to bf16 (round to nearest even)
-//               and TMA-stores through swizzled staging panels (predicated
-//               row stores where the tile straddles M).
+//               and TMA-stores through a swizzled staging panel, one 64-column
+//               panel after the other (predicated row stores where the tile
+//               straddles M).
 //   warps 12-15 scale staging: the scale bytes of each K block go into a
 //               ring of tensor-memory slots, written by tcgen05.st (each
 //               warp its 32 lanes), eight K blocks per chunk, two chunks.
@@ -49,10 +50,14 @@
 
 namespace fp8g {
 
+#ifndef FP8G_UE8M0_STAGES
+#define FP8G_UE8M0_STAGES 4
+#endif
+
 struct Ue8m0Cfg {
     static constexpr int kBN = 256;
     static constexpr int kThreads = 512;            // 16 warps
-    static constexpr int kStages = 3;
+    static constexpr int kStages = FP8G_UE8M0_STAGES;
     static constexpr int kABytes = kBM * kBK;       // 16 KB
     static constexpr int kBBytes = kBN * kBK;       // 32 KB
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -64,7 +69,10 @@ struct Ue8m0Cfg {
     static constexpr int kPanelBytes = 32 * kPanelCols * 2;
     static constexpr int kColsPerWarp = kBN / 2;    // two drain warps per TMEM lane quarter
     static constexpr int kPanelsPerWarp = kColsPerWarp / kPanelCols;
-    static constexpr int kStagingBytes = kNumEpiWarps * kPanelsPerWarp * kPanelBytes;   // 64 KB
+    // staging panels per warp: with 4 operand stages one (the warp's two
+    // panels pass through it one after the other), else two
+    static constexpr int kStagingPanels = kStages >= 4 ? 1 : 2;
+    static constexpr int kStagingBytes = kNumEpiWarps * kStagingPanels * kPanelBytes;
     static constexpr int kBarriers = 2 * kStages + 2 + 2 * kChunks + 1;
     static constexpr int kSmemBytes =
         kStages * kStageBytes + kStagingBytes + kBarriers * 8 + 16 + 1024 /* alignment slack */;
@@ -243,7 +251,7 @@ __global__ void __launch_bounds__(Ue8m0Cfg::kThreads, 1)
         const int ew = warp - kEpiWarp0;
         const int q = warp & 3;
         const int h = ew >> 2;
-        uint8_t *panels = sm_stage_d + ew * C::kPanelsPerWarp * C::kPanelBytes;
+        uint8_t *panels = sm_stage_d + ew * C::kStagingPanels * C::kPanelBytes;
         Scheduler<BN, kKindNT, false> sched(p, false);
         Work w;
         uint32_t acc_ph = 0;
@@ -287,9 +295,17 @@ __global__ void __launch_bounds__(Ue8m0Cfg::kThreads, 1)
             if (rows_ok > 0) {
                 if (x < p.N)
                     store_panel_packed<C::kPanelCols>(pk0, panels, &tmap_d, p, x, y_row0, rows_ok, lane);
-                if (x + C::kPanelCols < p.N)
-                    store_panel_packed<C::kPanelCols>(pk1, panels + C::kPanelBytes, &tmap_d, p, x + C::kPanelCols,
-                                                      y_row0, rows_ok, lane);
+                if (x + C::kPanelCols < p.N) {
+                    uint8_t *second = panels + (C::kStagingPanels - 1) * C::kPanelBytes;
+                    if (C::kStagingPanels == 1) {
+                        // one panel buffer: the first panel's store has read it
+                        if (lane == 0)
+                            bulk_wait_group_read<0>();
+                        __syncwarp();
+                    }
+                    store_panel_packed<C::kPanelCols>(pk1, second, &tmap_d, p, x + C::kPanelCols, y_row0, rows_ok,
+                                                      lane);
+                }
             }
         }
         if (lane == 0)
