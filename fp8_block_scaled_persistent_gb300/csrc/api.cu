@@ -35,7 +35,9 @@ __device__ int g_error_word;              // sticky device-side error bits, per 
 
 std::atomic<int> g_override_bn{0};
 std::atomic<int> g_override_split{0};
-// CTA-pair kernel: 0 = automatic choice, 1 = wherever it applies, -1 = never
+// CTA pairs: 0 = automatic choice, 1 = the cta_group::2 pair kernel wherever
+// it applies, 2 = clusters of two one-CTA kernels sharing A over DSMEM,
+// -1 = never
 std::atomic<int> g_override_pair{0};
 
 // FP8G_FORCE_CONFIG="block_n[,split_ctas]" sets the tuning overrides when the
@@ -65,7 +67,7 @@ struct EnvOverride {
     }
 } g_env_override;
 
-// FP8G_PAIR_MODE="-1" | "0" | "1" sets the CTA-pair choice when the library
+// FP8G_PAIR_MODE="-1" | "0" | "1" | "2" sets the CTA-pair choice when the library
 // loads (the values fp8_gemm_set_pair_mode accepts); anything else is ignored.
 struct EnvPairMode {
     EnvPairMode()
@@ -79,6 +81,8 @@ struct EnvPairMode {
             g_override_pair.store(0);
         else if (!std::strcmp(v, "1"))
             g_override_pair.store(1);
+        else if (!std::strcmp(v, "2"))
+            g_override_pair.store(2);
     }
 } g_env_pair_mode;
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
@@ -374,7 +378,7 @@ int pair_bn() { return g_override_bn.load() ? g_override_bn.load() : 256; }
 bool want_pair(long long pair_tiles, const DeviceInfo &dev, int &pairs)
 {
     const int mode = g_override_pair.load();
-    if (mode < 0 || pair_tiles <= 0)
+    if (mode < 0 || mode == 2 || pair_tiles <= 0)
         return false;
     pairs = fp8g::max_active_pairs(dev.id, pair_bn());
     if (pairs <= 0)
@@ -382,6 +386,39 @@ bool want_pair(long long pair_tiles, const DeviceInfo &dev, int &pairs)
     if (mode > 0)
         return true;
     return kPairAuto && pair_tiles >= pairs;
+}
+
+// Whether an unsplit launch runs as clusters of two CTAs sharing A over DSMEM
+// (only when asked for: fp8_gemm_set_pair_mode(2)), and over how many
+// clusters.  Tiles are 128 x 256; `share_tiles` counts (m-block, pair of
+// n-blocks) tiles.
+bool want_share(long long share_tiles, const DeviceInfo &dev, int &pairs)
+{
+    if (g_override_pair.load() != 2 || share_tiles <= 0)
+        return false;
+    const int obn = g_override_bn.load();
+    if (obn != 0 && obn != 256)
+        return false;
+    pairs = fp8g::max_active_share_pairs(dev.id);
+    return pairs > 0;
+}
+
+int share_n_pairs(int N) { return (ceil_div(N, 256) + 1) / 2; }
+
+// The plain GEMM as A-sharing clusters (no split, no addend).
+int run_nt_share(const void *A, const float *SFA, const void *B, const float *SFB, void *D, int M, int N, int K,
+                 int pairs, const DeviceInfo &dev, fp8g_stream_t stream)
+{
+    LaunchArgs a;
+    fill_common(a.p, M, N, K, 1, SFA, SFB, D, nullptr, 256, dev);
+    a.p.num_m_blocks = ceil_div(M, 128);
+    a.p.group_m = 8;
+    a.p.num_tiles = a.p.num_m_blocks * share_n_pairs(N);
+    if (!make_maps(a, A, SFA, B, SFB, D, M, N, M, a.p.kb, a.p.sfa_ld, (long long)a.p.nb * a.p.kb, N, K, 256))
+        return FP8G_ERR_CUDA;
+    a.grid = 2 * std::min(pairs, a.p.num_tiles);
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    return to_status(fp8g::launch_share(fp8g::kKindNT, a));
 }
 
 // The plain GEMM on CTA pairs (no split), with or without the addend C.
@@ -419,6 +456,8 @@ int run_nt(const void *A, const float *SFA, const void *B, const float *SFB, con
     int pairs = 0;
     if (!c.split_ctas && want_pair((long long)ceil_div(M, 256) * ceil_div(N, pair_bn()), dev, pairs))
         return run_nt_pair(A, SFA, B, SFB, C, D, M, N, K, pairs, dev, stream);
+    if (!c.split_ctas && !C && want_share((long long)ceil_div(M, 128) * share_n_pairs(N), dev, pairs))
+        return run_nt_share(A, SFA, B, SFB, D, M, N, K, pairs, dev, stream);
 
     LaunchArgs a;
     fill_common(a.p, M, N, K, 1, SFA, SFB, D, nullptr, c.block_n, dev);
@@ -515,6 +554,19 @@ int fp8_gemm_grouped_contiguous(const void *A, const float *SFA, const void *B, 
         a.stream = reinterpret_cast<cudaStream_t>(stream);
         return to_status(fp8g::launch_pair(fp8g::kKindContiguous, bn, a));
     }
+    if (want_share((long long)(M_total / 128) * share_n_pairs(N), dev, pairs)) {
+        LaunchArgs a;
+        fill_common(a.p, M_total, N, K, G, SFA, SFB, D, m_indices, 256, dev);
+        a.p.num_m_blocks = M_total / 128;
+        a.p.group_m = 8;
+        a.p.num_tiles = a.p.num_m_blocks * share_n_pairs(N);
+        if (!make_maps(a, A, SFA, B, SFB, D, M_total, (long long)G * N, M_total, a.p.kb, a.p.sfa_ld,
+                       (long long)G * a.p.nb * a.p.kb, N, K, 256))
+            return FP8G_ERR_CUDA;
+        a.grid = 2 * std::min(pairs, a.p.num_tiles);
+        a.stream = reinterpret_cast<cudaStream_t>(stream);
+        return to_status(fp8g::launch_share(fp8g::kKindContiguous, a));
+    }
     const int mb = M_total / 128;
     const int block_n = pick_block_n(N, (long long)mb * ceil_div(N, 256) >= dev.sms);
     LaunchArgs a;
@@ -564,6 +616,19 @@ int fp8_gemm_grouped_masked(const void *A, const float *SFA, const void *B, cons
         a.grid = 2 * (int)std::min<long long>(pairs, tiles_max);
         a.stream = reinterpret_cast<cudaStream_t>(stream);
         return to_status(fp8g::launch_pair(fp8g::kKindMasked, bn, a));
+    }
+    if (want_share((long long)G * ceil_div(M_max, 128) * share_n_pairs(N), dev, pairs)) {
+        LaunchArgs a;
+        fill_common(a.p, M_max, N, K, G, SFA, SFB, D, masked_m, 256, dev);
+        a.p.num_m_blocks = ceil_div(M_max, 128);
+        a.p.group_m = a.p.num_m_blocks;
+        const long long tiles_max = (long long)G * a.p.num_m_blocks * share_n_pairs(N);
+        if (!make_maps(a, A, SFA, B, SFB, D, (long long)G * M_max, (long long)G * N, (long long)G * M_max,
+                       (long long)G * a.p.kb, a.p.sfa_ld, (long long)G * a.p.nb * a.p.kb, N, K, 256))
+            return FP8G_ERR_CUDA;
+        a.grid = 2 * (int)std::min<long long>(pairs, tiles_max);
+        a.stream = reinterpret_cast<cudaStream_t>(stream);
+        return to_status(fp8g::launch_share(fp8g::kKindMasked, a));
     }
     const int mb = ceil_div(M_max, 128);
     const long long tiles_max256 = (long long)G * mb * ceil_div(N, 256);
@@ -692,7 +757,7 @@ int fp8_gemm_set_override(int block_n, int split_ctas)
 
 int fp8_gemm_set_pair_mode(int mode)
 {
-    if (mode < -1 || mode > 1)
+    if (mode < -1 || mode > 2)
         return FP8G_ERR_INVALID_ARG;
     g_override_pair.store(mode);
     return FP8G_OK;
@@ -781,6 +846,8 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const float *SFA, const void *
     int pairs = 0;
     if (!c.split_ctas && want_pair((long long)ceil_div(M, 256) * ceil_div(N, pair_bn()), dev, pairs))
         return run_nt_pair(A, SFA, B, SFB, nullptr, D, M, N, K, pairs, dev, stream);
+    if (!c.split_ctas && want_share((long long)ceil_div(M, 128) * share_n_pairs(N), dev, pairs))
+        return run_nt_share(A, SFA, B, SFB, D, M, N, K, pairs, dev, stream);
     const size_t counters = ((size_t)c.tiles * 8 * sizeof(int) + 255) / 256 * 256;
 
     LaunchArgs a;

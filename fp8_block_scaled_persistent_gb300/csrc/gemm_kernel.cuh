@@ -153,7 +153,12 @@ __device__ __forceinline__ void raster(int t, int mb, int nbk, int group_m, int 
 
 // The tile sequence of one CTA.  Every role of the CTA runs its own copy and
 // sees the same sequence.
-template <int BN, int KIND, bool SPLIT>
+//
+// SHARE (clusters of two CTAs sharing the A tile over DSMEM): the tile index
+// runs over (m-block, pair of n-blocks) and the two CTAs of a cluster take
+// the same one, rank r computing n-block 2j + r; a rank whose n-block lies
+// past N computes on whatever B its view holds and stores nothing.
+template <int BN, int KIND, bool SPLIT, bool SHARE = false>
 struct Scheduler {
     const Params &p;
     int next_tile;
@@ -163,12 +168,17 @@ struct Scheduler {
 
     __device__ Scheduler(const Params &pp, bool report_bad_groups) : p(pp), report(report_bad_groups)
     {
-        next_tile = blockIdx.x;
+        next_tile = SHARE ? (int)blockIdx.x / 2 : (int)blockIdx.x;
         if constexpr (SPLIT) {
             u = unit_begin(blockIdx.x);
             u_end = unit_begin(blockIdx.x + 1);
         }
     }
+
+    __device__ __forceinline__ int stride() const { return SHARE ? (int)gridDim.x / 2 : (int)gridDim.x; }
+    __device__ __forceinline__ int n_cols() const { return SHARE ? (p.num_n_blocks + 1) / 2 : p.num_n_blocks; }
+    // the CTA's n-block of raster column c, and whether it lies inside N
+    __device__ __forceinline__ int n_of(int c) const { return SHARE ? 2 * c + (int)cluster_ctarank() : c; }
 
     // the host keeps units * CTAs below 2^31
     __device__ __forceinline__ int unit_begin(int c) const
@@ -207,20 +217,22 @@ struct Scheduler {
             if (next_tile >= p.num_tiles)
                 return false;
             const int t = next_tile;
-            next_tile += gridDim.x;
-            raster(t, p.num_m_blocks, p.num_n_blocks, p.group_m, w.m_blk, w.n_blk);
+            next_tile += stride();
+            raster(t, p.num_m_blocks, n_cols(), p.group_m, w.m_blk, w.n_blk);
+            w.n_blk = n_of(w.n_blk);
             w.g = 0;
             w.tile = t;
             w.kb0 = 0;
             w.kb1 = p.kb;
             w.a_row0 = w.m_blk * kBM;
-            w.valid_rows = min(kBM, p.rows - w.a_row0);
+            w.valid_rows = w.n_blk < p.num_n_blocks ? min(kBM, p.rows - w.a_row0) : 0;
             return true;
         } else if constexpr (KIND == kKindContiguous) {
             while (next_tile < p.num_tiles) {
                 const int t = next_tile;
-                next_tile += gridDim.x;
-                raster(t, p.num_m_blocks, p.num_n_blocks, p.group_m, w.m_blk, w.n_blk);
+                next_tile += stride();
+                raster(t, p.num_m_blocks, n_cols(), p.group_m, w.m_blk, w.n_blk);
+                w.n_blk = n_of(w.n_blk);
                 const int g = __ldg(p.layout + (size_t)w.m_blk * kBM);
                 if (g < 0 || g >= p.G) {
                     if (g != -1 && report)
@@ -232,7 +244,7 @@ struct Scheduler {
                 w.kb0 = 0;
                 w.kb1 = p.kb;
                 w.a_row0 = w.m_blk * kBM;
-                w.valid_rows = kBM;
+                w.valid_rows = w.n_blk < p.num_n_blocks ? kBM : 0;
                 return true;
             }
             return false;
@@ -243,7 +255,7 @@ struct Scheduler {
                     return false;
                 if (walk_tiles < 0) {
                     walk_count = clamp_count(walk_g);
-                    walk_tiles = ((walk_count + kBM - 1) / kBM) * p.num_n_blocks;
+                    walk_tiles = ((walk_count + kBM - 1) / kBM) * n_cols();
                 }
                 if (t < walk_base + walk_tiles)
                     break;
@@ -251,15 +263,16 @@ struct Scheduler {
                 walk_tiles = -1;
                 ++walk_g;
             }
-            next_tile += gridDim.x;
+            next_tile += stride();
             const int mb = (walk_count + kBM - 1) / kBM;
-            raster(t - walk_base, mb, p.num_n_blocks, p.group_m, w.m_blk, w.n_blk);
+            raster(t - walk_base, mb, n_cols(), p.group_m, w.m_blk, w.n_blk);
+            w.n_blk = n_of(w.n_blk);
             w.g = walk_g;
             w.tile = t;
             w.kb0 = 0;
             w.kb1 = p.kb;
             w.a_row0 = walk_g * p.rows + w.m_blk * kBM;
-            w.valid_rows = min(kBM, walk_count - w.m_blk * kBM);
+            w.valid_rows = w.n_blk < p.num_n_blocks ? min(kBM, walk_count - w.m_blk * kBM) : 0;
             return true;
         }
     }
@@ -458,7 +471,17 @@ __device__ __forceinline__ void add_c_half(float (&acc)[COLS], const uint8_t *st
 // ----------------------------------------------------------------------------
 // The kernel
 
-template <int BN, int KIND, bool SPLIT>
+// SHARE: launched in clusters of two CTAs that compute neighbouring n-blocks
+// of the same m-block (so the same A tiles; the TVM TIRx "copy_async ->
+// dsmem" page's two-CTA shared-to-shared bulk copy, used as the one-GPU
+// alternative to the multicast of the DeepGEMM page's tma_copy).  Rank 0
+// loads each A tile from global memory; its warp 2 forwards it into rank 1's
+// shared memory with one cp.async.bulk.shared::cluster, counted on rank 1's
+// full barrier.  Each CTA loads its own B.  Both MMA issuers commit to the
+// stage's empty barrier of both CTAs (count 2), so a stage is refilled only
+// once both CTAs' MMAs -- and hence the forward, which rank 1's MMA waited
+// for -- are done with it.
+template <int BN, int KIND, bool SPLIT, bool SHARE = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_sfa,
@@ -467,6 +490,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 {
 #if defined(__CUDA_ARCH__)
     using C = Cfg<BN>;
+    static_assert(!SHARE || (!SPLIT && !C::kPairLoads), "A sharing: unsplit schedules, one K block per copy");
     constexpr int S = C::kStages;
     constexpr int NACC = C::kAccBufs;
     constexpr int SR = C::kScaleSlots;
@@ -492,10 +516,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    const uint32_t rank = SHARE ? cluster_ctarank() : 0u;
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(&empty[i], SHARE ? 2 : 1);   // both CTAs' MMA commits when sharing
         }
         for (int i = 0; i < NACC; ++i)
             mbar_init(&tempty[i], kNumEpiWarps);
@@ -525,6 +550,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (SHARE)
+        cluster_sync();     // the peer's barriers exist before anything reaches them
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     // Launched as a programmatic dependent of the previous kernel on the
@@ -535,7 +562,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     grid_dependency_wait();
     grid_launch_dependents();
 
-    const WaitCtl ctl{abort_flag, p.error_word, p.timeout_ns};
+    const WaitCtl ctl{abort_flag, p.error_word, p.timeout_ns,
+                      SHARE ? mapa_shared(smem_u32(const_cast<int *>(abort_flag)), rank ^ 1u) : 0u};
 
     // Each role sits inside the branch that sets its register budget, so the
     // epilogue is only reachable with the larger one.
@@ -543,7 +571,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         regs_dealloc<kRegsCtl>();
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------ TMA producer
-            Scheduler<BN, KIND, SPLIT> sched(p, false);
+            Scheduler<BN, KIND, SPLIT, SHARE> sched(p, false);
             Work w;
             Ring ring, sring;
             uint32_t issued = 0, issued_parity = 0, sissued = 0, sissued_parity = 0;
@@ -576,8 +604,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             issued |= 2u << ring.i;
                             issued_parity = (issued_parity & ~(2u << ring.i)) | (ring.ph << (ring.i + 1));
                         } else {
+                            // when sharing, rank 1's A arrives from rank 0 (same byte count)
                             mbar_arrive_expect_tx(&full[ring.i], C::kStageBytes);
-                            tma_load_2d(sm_a + ring.i * C::kABytes, &tmap_a, &full[ring.i], k * kBK, w.a_row0);
+                            if (!SHARE || rank == 0)
+                                tma_load_2d(sm_a + ring.i * C::kABytes, &tmap_a, &full[ring.i], k * kBK, w.a_row0);
                             tma_load_2d(sm_b + ring.i * C::kBBytes, &tmap_b, &full[ring.i], k * kBK, b_row0);
                         }
                         issued |= 1u << ring.i;
@@ -613,9 +643,31 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             for (int i = 0; i < SR; ++i)
                 if (sissued & (1u << i))
                     mbar_wait_drain(&sfull[i], (sissued_parity >> i) & 1u, p.timeout_ns);
+        } else if (SHARE && warp == 2 && lane == 0 && rank == 0) {
+            // ------------------------------------------------ A forwarder (rank 0 of a sharing pair)
+            // once a stage's tiles have landed here, copy its A tile into the
+            // same stage of rank 1; the stage cannot be refilled before rank 1's
+            // MMA (which waits for this copy) is done with it
+            Scheduler<BN, KIND, SPLIT, SHARE> sched(p, false);
+            Work w;
+            Ring ring;
+            const uint32_t peer_a = mapa_shared(smem_u32(sm_a), 1);
+            const uint32_t peer_full = mapa_shared(smem_u32(full), 1);
+            bool ok = true;
+            while (ok && sched.next(w)) {
+                for (int k = w.kb0; k < w.kb1; ++k) {
+                    if (!mbar_wait(&full[ring.i], ring.ph, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    bulk_copy_to_cluster(peer_a + ring.i * C::kABytes, sm_a + ring.i * C::kABytes, C::kABytes,
+                                         peer_full + 8u * ring.i);
+                    ring.template next<S>();
+                }
+            }
         } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------ MMA issuer
-            Scheduler<BN, KIND, SPLIT> sched(p, false);
+            Scheduler<BN, KIND, SPLIT, SHARE> sched(p, false);
             Work w;
             Ring ring, acc;
             constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
@@ -639,8 +691,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         mma_f8f6f4(d_tmem, a0 + 2 * kk, b0 + 2 * kk, idesc, kk > 0 ? 1u : 0u);
                     // One commit per K block (each commit drains the tensor
                     // pipe): it frees the operand stage for the producer and
-                    // tells the epilogue that TMEM buffer acc.i is complete.
-                    mma_commit(&empty[ring.i]);
+                    // tells the epilogue that TMEM buffer acc.i is complete
+                    // (when sharing, in both CTAs of the pair).
+                    if constexpr (SHARE)
+                        mma_commit_multicast(&empty[ring.i], 0x3);
+                    else
+                        mma_commit(&empty[ring.i]);
                     second = pair;
                     ring.template next<S>();
                     acc.template next<NACC>();
@@ -670,7 +726,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
         }
 
-        Scheduler<BN, KIND, SPLIT> sched(p, ew == 0 && lane == 0);
+        Scheduler<BN, KIND, SPLIT, SHARE> sched(p, ew == 0 && lane == 0 && rank == 0);
         Work w;
         Ring ring, acc_ring, sring;
         bool ok = true;
@@ -865,6 +921,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (SHARE) {
+        // no commit, forwarded tile or abort store reaches either CTA after this
+        cluster_sync();
+        if (__syncthreads_or(*abort_flag)) {
+            // an aborted pair may have stopped with a forwarded tile in flight
+            // that no barrier it still waits on counts: give it time to land
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 200000ull)
+                __nanosleep(1000);
+        }
+    }
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, kTmemCols);

@@ -42,6 +42,14 @@ int pair_panel_cols();
 // Clusters of two that can be resident at once on device `dev` (0 on failure).
 int max_active_pairs(int dev, int block_n);
 
+// The one-CTA kernel in clusters of two sharing each A tile over DSMEM
+// (gemm_share.cu): 256-column tiles, unsplit; `kind` is kKindNT,
+// kKindContiguous or kKindMasked; the tensor maps are make_maps' for
+// block_n 256; a.p.num_tiles counts (m-block, pair of n-blocks) tiles and
+// a.grid is twice the number of clusters.
+cudaError_t launch_share(int kind, const LaunchArgs &a);
+int max_active_share_pairs(int dev);
+
 // The power-of-two-scale kernel (gemm_ue8m0.cu): tiles of 128 x
 // ue8m0_block_n(), a.p.sfa_e / a.p.sfb_e set; tensor maps tmap_a (boxes of
 // 128 rows), tmap_b (boxes of ue8m0_block_n() rows), tmap_d (panels of

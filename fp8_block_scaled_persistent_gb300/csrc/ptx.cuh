@@ -535,6 +535,32 @@ __device__ __forceinline__ void st_cg_f4(float4 *p, float4 v)
                  : "memory");
 }
 
+// ---------------------------------------------------------------- sharing over DSMEM
+
+// Copies `bytes` (a multiple of 16) from this CTA's shared memory to the
+// shared memory of a CTA of the cluster (a shared::cluster address); the
+// bytes are counted on an mbarrier of the destination CTA.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster_addr, const void *src, uint32_t bytes,
+                                                     uint32_t bar_cluster_addr)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_cluster_addr),
+                 "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster_addr)
+                 : "memory");
+}
+
+// Arrives once on the mbarrier at the same shared-memory offset as `bar` in
+// every CTA of `cta_mask` when the MMAs this thread issued so far have
+// completed (one-CTA MMAs).
+__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- block-scaled MMA (power-of-two scales)
 
 // D(tmem) (+)= (A * 2^(sa-127)) (B * 2^(sb-127))^T, E4M3 x E4M3 -> F32,

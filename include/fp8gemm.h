@@ -211,11 +211,19 @@ int fp8_gemm_set_override(int block_n, int split_ctas);
  *             (each CTA loads its own 128 rows of A and half of the tile's B;
  *             nothing is multicast) -- unless a block_n override other than
  *             128 is set;
+ *   mode  2 : run every unsplit plain, contiguous and masked call (not the
+ *             addend variant) with 128 x 256 tiles in clusters of two CTAs
+ *             that compute neighbouring n-blocks of one m-block: the first
+ *             CTA loads each A tile and copies it into the second one's
+ *             shared memory (cp.async.bulk.shared::cluster), so the pair
+ *             reads A from global memory once.  A block_n override other than
+ *             256 turns it off.  Source: TVM TIRx, the "copy_async -> dsmem"
+ *             two-CTA shared-to-shared bulk copy;
  *   mode  0 : the automatic choice (the default);
  *   mode -1 : never use CTA pairs.
  * Results are the same to within fp32 rounding order (bit-identical on
  * exactly representable inputs).  Returns FP8G_ERR_INVALID_ARG for other
- * values.  The environment variable FP8G_PAIR_MODE ("-1", "0" or "1"), read
+ * values.  The environment variable FP8G_PAIR_MODE ("-1", "0", "1" or "2"), read
  * when the library loads, sets the same value; this call replaces it.
  * Source of the sharing: DeepGEMM fp8_gemm.cuh, tma_copy<kNumTMAMulticast>
  * and the cluster launch of Gemm::run (the pages share one m-block's A across
