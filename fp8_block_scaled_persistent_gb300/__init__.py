@@ -16,6 +16,9 @@ import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8gemm.so")
+# the bounds-checking build (every kernel compiled with FP8G_DEBUG_BOUNDS=1);
+# FP8G_LIBRARY=debug in the environment makes library() load it instead
+DEBUG_LIB_PATH = os.path.join(_HERE, "libfp8gemm_debug.so")
 
 FP8G_OK = 0
 FP8G_ERR_INVALID_ARG = 1
@@ -26,6 +29,7 @@ FP8G_ERR_TIMEOUT = 5
 FP8G_ERR_BAD_GROUP = 6
 FP8G_ERR_WORKSPACE = 7
 FP8G_ERR_SCRATCH_LIMIT = 8
+FP8G_ERR_BOUNDS = 9
 
 FP8G_KIND_NT = 0
 FP8G_KIND_GROUPED_CONTIGUOUS = 1
@@ -50,9 +54,12 @@ class Fp8GemmError(RuntimeError):
         super().__init__(f"{what}: status {status} ({status_string(status)})")
 
 
-def library(path: str = LIB_PATH):
-    """The loaded C library (raises if it has not been built)."""
+def library(path: str | None = None):
+    """The loaded C library (raises if it has not been built).  The
+    bounds-checking build is loaded instead when FP8G_LIBRARY=debug."""
     global _lib
+    if path is None:
+        path = DEBUG_LIB_PATH if os.environ.get("FP8G_LIBRARY") == "debug" else LIB_PATH
     with _lock:
         if _lib is not None:
             return _lib

@@ -40,33 +40,49 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
-    cc = nvcc()
+# the bounds-checking build: every kernel checks the invariants its accesses
+# rely on and records FP8G_ERR_BOUNDS instead of faulting (see ptx.cuh)
+DEBUG_LIB = os.path.join(PKG, "libfp8gemm_debug.so")
+DEBUG_FLAGS = ["-DFP8G_DEBUG_BOUNDS=1"]
 
-    def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [cc, *NVCC_FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
+
+def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+    """Builds libfp8gemm.so and its bounds-checking twin libfp8gemm_debug.so
+    (all translation units of both compiled in parallel); returns the path of
+    the first."""
+    deps = _deps_mtime()
+    if (not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= deps and os.path.exists(DEBUG_LIB)
+            and os.path.getmtime(DEBUG_LIB) >= deps):
+        return LIB
+    cc = nvcc()
+    jobs = [(src, BUILD, list(extra_flags)) for src in SOURCES] + \
+           [(src, os.path.join(BUILD, "debug"), DEBUG_FLAGS + list(extra_flags)) for src in SOURCES]
+    for d in {j[1] for j in jobs}:
+        os.makedirs(d, exist_ok=True)
+
+    def compile_one(job):
+        src, outdir, flags = job
+        obj = os.path.join(outdir, os.path.splitext(src)[0] + ".o")
+        cmd = [cc, *NVCC_FLAGS, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+            raise RuntimeError(f"nvcc failed on {src} ({' '.join(flags)}):\n{r.stdout}\n{r.stderr}")
         if verbose:
             sys.stderr.write(r.stdout + r.stderr)
         return obj, r.stderr
 
-    with ThreadPoolExecutor(len(SOURCES)) as ex:
-        done = list(ex.map(compile_one, SOURCES))
-    objs = [o for o, _ in done]
-    # the register report of every kernel (checked by tests/test_build.py)
+    with ThreadPoolExecutor(min(len(jobs), max(4, os.cpu_count() or 4))) as ex:
+        done = list(ex.map(compile_one, jobs))
+    n = len(SOURCES)
+    # the register report of every kernel of the normal build (checked by tests/test_build.py)
     with open(PTXAS_LOG, "w") as f:
-        f.write("".join(log for _, log in done))
-    tmp = LIB + f".tmp{os.getpid()}"
-    r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+        f.write("".join(log for _, log in done[:n]))
+    for lib, objs in ((LIB, [o for o, _ in done[:n]]), (DEBUG_LIB, [o for o, _ in done[n:]])):
+        tmp = lib + f".tmp{os.getpid()}"
+        r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, lib)
     return LIB
 
 

@@ -315,6 +315,10 @@ void fill_common(Params &p, long long rows, int N, int K, int G, const float *SF
     p.num_n_blocks = ceil_div(N, block_n);
     p.error_word = dev.error_word;
     p.timeout_ns = g_timeout_ns.load();
+    // 2-D view extents (the masked launch paths scale A's and D's by G)
+    p.a_rows_total = (int)rows;
+    p.d_rows_total = (int)rows;
+    p.b_rows_total = (int)((long long)G * N);
 }
 
 // The TMA swizzle that matches a staging panel's row width (2 bytes a column).
@@ -607,6 +611,7 @@ int fp8_gemm_grouped_masked(const void *A, const float *SFA, const void *B, cons
         const int bn = pair_bn();
         LaunchArgs a;
         fill_common(a.p, M_max, N, K, G, SFA, SFB, D, masked_m, bn, dev);
+        a.p.a_rows_total = a.p.d_rows_total = (int)((long long)G * M_max);
         a.p.num_m_blocks = ceil_div(M_max, 256);
         a.p.group_m = a.p.num_m_blocks;
         const long long tiles_max = (long long)G * a.p.num_m_blocks * a.p.num_n_blocks;
@@ -620,6 +625,7 @@ int fp8_gemm_grouped_masked(const void *A, const float *SFA, const void *B, cons
     if (want_share((long long)G * ceil_div(M_max, 128) * share_n_pairs(N), dev, pairs)) {
         LaunchArgs a;
         fill_common(a.p, M_max, N, K, G, SFA, SFB, D, masked_m, 256, dev);
+        a.p.a_rows_total = a.p.d_rows_total = (int)((long long)G * M_max);
         a.p.num_m_blocks = ceil_div(M_max, 128);
         a.p.group_m = a.p.num_m_blocks;
         const long long tiles_max = (long long)G * a.p.num_m_blocks * share_n_pairs(N);
@@ -635,6 +641,7 @@ int fp8_gemm_grouped_masked(const void *A, const float *SFA, const void *B, cons
     const int block_n = pick_block_n(N, tiles_max256 >= dev.sms);
     LaunchArgs a;
     fill_common(a.p, M_max, N, K, G, SFA, SFB, D, masked_m, block_n, dev);
+    a.p.a_rows_total = a.p.d_rows_total = (int)((long long)G * M_max);
     a.p.num_m_blocks = mb;
     a.p.group_m = mb;   // all m-blocks of a (group, n-block) run together: B is read once
     const long long tiles_max = (long long)G * mb * a.p.num_n_blocks;
@@ -720,6 +727,8 @@ int fp8_gemm_get_device_error(fp8g_stream_t stream)
         if (cudaMemcpy(dev.error_word, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
             return FP8G_ERR_CUDA;
     }
+    if (v & fp8g::kErrBoundsBit)
+        return FP8G_ERR_BOUNDS;
     if (v & fp8g::kErrTimeoutBit)
         return FP8G_ERR_TIMEOUT;
     if (v & fp8g::kErrBadGroupBit)
@@ -740,6 +749,7 @@ const char *fp8_gemm_status_string(int status)
     case FP8G_ERR_WORKSPACE: return "workspace too small for the forced split";
     case FP8G_ERR_SCRATCH_LIMIT:
         return "problem needs more split-K scratch than fp8_gemm_nt_noalloc's static buffer holds";
+    case FP8G_ERR_BOUNDS: return "a device-side bounds check failed (bounds-checking build)";
     default: return "unknown status";
     }
 }

@@ -578,6 +578,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             bool second = false;    // this K block's operands came with the previous block's
             bool ok = true;
             while (ok && sched.next(w)) {
+                // the work unit lies inside the problem (the bounds-checking build)
+                if (!bounds_ok(w.g >= 0 && w.g < p.G && w.kb0 >= 0 && w.kb0 < w.kb1 && w.kb1 <= p.kb &&
+                                   w.a_row0 >= 0 && w.a_row0 < p.a_rows_total && w.n_blk >= 0 &&
+                                   (w.valid_rows == 0 || (w.n_blk * BN < p.N && w.valid_rows <= kBM)),
+                               ctl)) {
+                    ok = false;
+                    break;
+                }
                 const int b_row0 = w.g * p.N + w.n_blk * BN;
                 const int sfa_y0 = (KIND == kKindMasked) ? w.g * p.kb : 0;
                 const int sfb_x0 = (w.g * p.nb + (w.n_blk * BN) / 128) * p.kb;
@@ -743,6 +751,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int c_rows = (kStagedC && w.kb1 == p.kb) ? min(max(w.valid_rows - 32 * q, 0), 32) : 0;
             const bool c_early = w.kb1 - w.kb0 >= 8;
             const int k_copy0 = w.kb0 + 3, k_add0 = w.kb1 - 3;
+            if (KIND == kKindNTAcc &&
+                !bounds_ok(w.a_row0 + w.valid_rows <= p.rows && w.n_blk * BN < p.N, ctl)) {
+                ok = false;
+                break;
+            }
             if constexpr (KIND == kKindNTAcc && !C::kFullTileStaging) {
                 init_from_c<BN, COLS>(acc, p, w, q, h, lane);
             } else {
@@ -833,6 +846,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                ((size_t)slot_of(c) * kNumEpiWarps + ew) * F4 * 32;
                     };
                     int *ctr = p.counters + (size_t)t * kNumEpiWarps + ew;
+                    if (!bounds_ok(t >= 0 && t < p.num_tiles && c_lo >= 0 && c_lo <= (int)blockIdx.x &&
+                                       (int)blockIdx.x <= c_hi && c_hi < P && slot_of((int)blockIdx.x) < 2 * P,
+                                   ctl)) {
+                        ok = false;
+                        break;
+                    }
                     if ((int)blockIdx.x != c_hi) {
                         float4 *mine = region(blockIdx.x);
 #pragma unroll
@@ -875,8 +894,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
 
             // ---- bf16 store of this warp's 32 rows x COLS columns
-            const int rows_ok = has_out ? min(max(w.valid_rows - 32 * q, 0), 32) : 0;
+            int rows_ok = has_out ? min(max(w.valid_rows - 32 * q, 0), 32) : 0;
             const int y_row0 = w.a_row0 + 32 * q;
+            if (rows_ok > 0 && !bounds_ok(y_row0 >= 0 && y_row0 + rows_ok <= p.d_rows_total, ctl))
+                rows_ok = 0;
             if constexpr (C::kFullTileStaging) {
                 // the previous tile's stores have had a whole tile to read
                 // this warp's staging area; make sure they are done

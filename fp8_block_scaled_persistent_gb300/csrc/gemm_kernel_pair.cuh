@@ -325,6 +325,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t issued = 0, issued_parity = 0, sissued = 0, sissued_parity = 0;
             bool ok = true;
             while (ok && sched.next(w)) {
+                if (!bounds_ok(w.g >= 0 && w.g < p.G && w.n_blk >= 0 && w.n_blk * BN < p.N && w.a_row0 >= 0 &&
+                                   (w.valid_rows == 0 || (w.a_row0 < p.a_rows_total && w.valid_rows <= kBM)),
+                               ctl)) {
+                    ok = false;
+                    break;
+                }
                 const int b_row0 = w.g * p.N + w.n_blk * BN + rank * C::kBHalfRows;
                 const int sfa_y0 = (KIND == kKindMasked) ? w.g * p.kb : 0;
                 const int sfb_x0 = (w.g * p.nb + (w.n_blk * BN) / 128) * p.kb;
@@ -426,6 +432,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         bool ok = true;
         while (ok && sched.next(w)) {
             float acc[COLS];
+            if (KIND == kKindNTAcc && !bounds_ok(w.a_row0 + w.valid_rows <= p.rows || w.valid_rows == 0, ctl)) {
+                ok = false;
+                break;
+            }
             if constexpr (KIND == kKindNTAcc) {
                 // the addend starts the accumulator (the only CTA of the tile)
                 Work w1;
@@ -477,8 +487,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 break;
 
             // ---- bf16 store of this warp's 32 rows x COLS columns
-            const int rows_ok = min(max(w.valid_rows - 32 * q, 0), 32);
+            int rows_ok = min(max(w.valid_rows - 32 * q, 0), 32);
             const int y_row0 = w.a_row0 + 32 * q;
+            if (rows_ok > 0 && !bounds_ok(y_row0 >= 0 && y_row0 + rows_ok <= p.d_rows_total, ctl))
+                rows_ok = 0;
             const int x = w.n_blk * BN + h * COLS;
             // the previous tile's store has had a whole tile to read this
             // warp's panel; make sure it has

@@ -180,6 +180,11 @@ __global__ void __launch_bounds__(Ue8m0Cfg::kThreads, 1)
         uint32_t issued = 0, issued_parity = 0;
         bool ok = true;
         while (ok && sched.next(w)) {
+            if (!bounds_ok(w.a_row0 >= 0 && w.a_row0 < p.a_rows_total && w.n_blk >= 0 && w.n_blk * BN < p.N,
+                           ctl)) {
+                ok = false;
+                break;
+            }
             const int b_row0 = w.n_blk * BN;
             for (int k = 0; k < p.kb; ++k) {
                 if (!mbar_wait(&empty[ring.i], ring.ph ^ 1u, ctl)) {
@@ -285,9 +290,11 @@ __global__ void __launch_bounds__(Ue8m0Cfg::kThreads, 1)
                     pk1[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
             }
             acc_ph ^= 1u;
-            const int rows_ok = min(max(w.valid_rows - 32 * q, 0), 32);
+            int rows_ok = min(max(w.valid_rows - 32 * q, 0), 32);
             const int y_row0 = w.a_row0 + 32 * q;
             const int x = w.n_blk * BN + h * C::kColsPerWarp;
+            if (rows_ok > 0 && !bounds_ok(y_row0 >= 0 && y_row0 + rows_ok <= p.d_rows_total, ctl))
+                rows_ok = 0;
             // the previous tile's stores have read this warp's panels
             if (lane == 0)
                 bulk_wait_group_read<0>();
@@ -323,6 +330,10 @@ __global__ void __launch_bounds__(Ue8m0Cfg::kThreads, 1)
             const bool row_ok = row < p.rows;
             const int nblk0 = 2 * w.n_blk;
             const bool nb1_ok = nblk0 + 1 < p.nb;
+            if (!bounds_ok(nblk0 >= 0 && nblk0 < p.nb && w.a_row0 >= 0, ctl)) {
+                ok = false;
+                break;
+            }
             for (int k0 = 0; k0 < p.kb; k0 += C::kChunk) {
                 const int n = min(C::kChunk, p.kb - k0);
                 int got = 1;

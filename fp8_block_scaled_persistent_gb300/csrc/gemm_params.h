@@ -11,7 +11,7 @@ namespace fp8g {
 enum Kind : int { kKindNT = 0, kKindContiguous = 1, kKindMasked = 2, kKindNTAcc = 3 };
 
 // Bits of the sticky device-side error word.
-enum : int { kErrTimeoutBit = 1, kErrBadGroupBit = 2 };
+enum : int { kErrTimeoutBit = 1, kErrBadGroupBit = 2, kErrBoundsBit = 4 };
 
 // K blocks whose scales one scale copy brings in: the A scales of 128 rows x
 // kScaleChunk K blocks (one 2-D box) and, per 128-column block, the B scales
@@ -40,6 +40,10 @@ struct Params {
     int *counters;     // split: num_tiles * 8 counters of published partials
     int *error_word;
     unsigned long long timeout_ns;
+    // extents of the 2-D views (rows), for the bounds-checking build
+    int a_rows_total;  // A: rows (masked: G * M_max)
+    int b_rows_total;  // B: G * N
+    int d_rows_total;  // D: rows (masked: G * M_max)
 };
 
 }  // namespace fp8g

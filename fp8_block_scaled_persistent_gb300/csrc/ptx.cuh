@@ -109,6 +109,31 @@ __device__ __forceinline__ void raise_abort(const WaitCtl &c)
     atomicOr(c.error_word, kErrTimeoutBit);
 }
 
+// The bounds-checking build (FP8G_DEBUG_BOUNDS=1): each kernel checks the
+// invariants its memory accesses rely on (a tile starts inside the problem,
+// indices of groups, K blocks, split slots and counters are in range, stores
+// stay inside D).  A failed check records kErrBoundsBit in the device error
+// word, raises the CTA's abort flag so that every role stops at its next
+// wait, and the access is skipped; nothing traps.  In the normal build the
+// checks compile away.
+#ifndef FP8G_DEBUG_BOUNDS
+#define FP8G_DEBUG_BOUNDS 0
+#endif
+__device__ __forceinline__ bool bounds_ok(bool cond, const WaitCtl &c)
+{
+#if FP8G_DEBUG_BOUNDS
+    if (!cond) {
+        atomicOr(c.error_word, kErrBoundsBit);
+        *c.abort_flag = 1;
+    }
+    return cond;
+#else
+    (void)c;
+    (void)cond;
+    return true;
+#endif
+}
+
 // Waits for the phase with the given parity to complete.  Returns false if the
 // wait ran out (the abort flag and the device error are then set) or if
 // another role of this CTA already aborted.  The clock is only read after 32

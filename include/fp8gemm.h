@@ -65,7 +65,8 @@ enum fp8g_status {
     FP8G_ERR_TIMEOUT = 5,      /* device: a bounded pipeline wait ran out     */
     FP8G_ERR_BAD_GROUP = 6,    /* device: group index / count out of range    */
     FP8G_ERR_WORKSPACE = 7,    /* workspace smaller than a forced split needs */
-    FP8G_ERR_SCRATCH_LIMIT = 8 /* fp8_gemm_nt_noalloc: static scratch too small */
+    FP8G_ERR_SCRATCH_LIMIT = 8, /* fp8_gemm_nt_noalloc: static scratch too small */
+    FP8G_ERR_BOUNDS = 9        /* device: a bounds check of the checking build failed */
 };
 
 enum fp8g_kind {
@@ -175,8 +176,13 @@ size_t fp8_gemm_workspace_size(int kind, int M, int N, int K, int G);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's sticky
- * device-side error (FP8G_OK if none; FP8G_ERR_TIMEOUT wins over
- * FP8G_ERR_BAD_GROUP).  FP8G_ERR_CUDA if the synchronisation itself failed.
+ * device-side error (FP8G_OK if none; FP8G_ERR_BOUNDS wins over
+ * FP8G_ERR_TIMEOUT, which wins over FP8G_ERR_BAD_GROUP).  FP8G_ERR_CUDA if the
+ * synchronisation itself failed.  FP8G_ERR_BOUNDS comes only from the
+ * bounds-checking build of this library (libfp8gemm_debug.so, compiled with
+ * FP8G_DEBUG_BOUNDS=1): its kernels check that every tile, group, K-block,
+ * split-slot and counter index and every store lies inside the problem, and
+ * skip the access (and stop the block) instead of faulting when one does not.
  */
 int fp8_gemm_get_device_error(fp8g_stream_t stream);
 

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(0, 8):
+    for s in range(0, 10):
         assert fg.fp8_gemm_status_string(s)
     assert fg.fp8_gemm_status_string(999) == "unknown status"
 
