@@ -42,7 +42,7 @@ def _ref(p):
 
 def test_pair_mode_argument_checks():
     import fp8_block_scaled_persistent_gb300 as fg
-    assert fg.fp8_gemm_set_pair_mode(2) == fg.FP8G_ERR_INVALID_ARG
+    assert fg.fp8_gemm_set_pair_mode(3) == fg.FP8G_ERR_INVALID_ARG
     assert fg.fp8_gemm_set_pair_mode(-2) == fg.FP8G_ERR_INVALID_ARG
 
 
