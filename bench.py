@@ -372,7 +372,7 @@ def run_ours(args, dist, ws, rank, local):
 
     # per-shape device times: each workload alone, at least MIN_SHAPE_LAUNCHES
     # launches back to back (eager, and replayed from a CUDA graph)
-    per_n = max(MIN_SHAPE_LAUNCHES, min(args.steps, 2000))
+    per_n = max(args.shape_launches, min(args.steps, 2000))
     timed = {}
     for n in shape_names:
         timed[n] = time_shape(fg, by_name[n], stream, per_n, dist, device)
@@ -736,6 +736,8 @@ def main(argv=None):
                     help="time only the headline workload(s), not every configuration")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of CPU oracle work for the cpu_baseline sample")
+    ap.add_argument("--shape-launches", type=int, default=MIN_SHAPE_LAUNCHES,
+                    help="launches per shape in the per-shape timing (profiling runs use a few)")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

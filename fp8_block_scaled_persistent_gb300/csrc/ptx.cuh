@@ -56,9 +56,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
 // One poll of the barrier phase.  FP8G_WAIT_MODE selects the form (a build
 // option for measurement): 0 = try_wait (may suspend the thread until the
 // phase completes or a system time limit passes), 1 = test_wait (never
-// suspends), 2 = try_wait with a 20 ns suspend-time hint.
+// suspends), 2 = try_wait with a suspend-time hint of FP8G_WAIT_HINT_NS.
 #ifndef FP8G_WAIT_MODE
 #define FP8G_WAIT_MODE 0
+#endif
+#ifndef FP8G_WAIT_HINT_NS
+#define FP8G_WAIT_HINT_NS 20
 #endif
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity)
 {
@@ -77,7 +80,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar_addr), "r"(parity), "r"(20)
+        : "r"(bar_addr), "r"(parity), "r"(FP8G_WAIT_HINT_NS)
         : "memory");
 #else
     asm volatile(
