@@ -825,7 +825,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
             bool has_out = true;
             if constexpr (SPLIT) {
-                if (!(w.kb0 == 0 && w.kb1 == p.kb)) {
+                // a warp whose 32 rows all lie past M (M <= 96) neither
+                // publishes nor reduces: every contributor of the tile sees the
+                // same rows, so the region's counter is simply never used
+                const bool warp_rows = w.valid_rows > 32 * q;
+                if (!warp_rows)
+                    has_out = false;
+                if (warp_rows && !(w.kb0 == 0 && w.kb1 == p.kb)) {
                     // split tile: contributors c_lo .. c_hi (CTA order) each
                     // hold the partial of their K range.  All but c_hi publish
                     // theirs for this warp's 32 x COLS region and bump the
