@@ -316,6 +316,7 @@ void fill_common(Params &p, long long rows, int N, int K, int G, const float *SF
     p.error_word = dev.error_word;
     p.timeout_ns = g_timeout_ns.load();
     // 2-D view extents (the masked launch paths scale A's and D's by G)
+    p.a_box_rows = 128;
     p.a_rows_total = (int)rows;
     p.d_rows_total = (int)rows;
     p.b_rows_total = (int)((long long)G * N);
@@ -337,7 +338,7 @@ bool make_maps(LaunchArgs &a, const void *A, const float *SFA, const void *B, co
                long long sfb_count, int N, int K, int block_n)
 {
     const int pc = fp8g::panel_cols_for(block_n);
-    return make_map(&a.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, a_rows, K, 128, 128,
+    return make_map(&a.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, a_rows, K, 128, (uint32_t)a.p.a_box_rows,
                     CU_TENSOR_MAP_SWIZZLE_128B) &&
            make_map(&a.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, b_rows, K, 128, block_n,
                     CU_TENSOR_MAP_SWIZZLE_128B) &&
@@ -466,6 +467,7 @@ int run_nt(const void *A, const float *SFA, const void *B, const float *SFB, con
     LaunchArgs a;
     fill_common(a.p, M, N, K, 1, SFA, SFB, D, nullptr, c.block_n, dev);
     a.p.c = C;
+    a.p.a_box_rows = M <= 64 ? 64 : 128;    // rows past M are never stored: load only the first 64
     a.p.num_m_blocks = ceil_div(M, 128);
     a.p.group_m = 8;
     a.p.num_tiles = c.tiles;

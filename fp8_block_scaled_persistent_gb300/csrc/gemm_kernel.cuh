@@ -599,21 +599,30 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             ok = false;
                             break;
                         }
+                        const uint32_t a_bytes = (uint32_t)p.a_box_rows * kBK;
                         if (pair) {
                             // both tiles signal the first stage's barrier; the
                             // second stage's barrier completes its phase with a
                             // plain arrival, so that every barrier keeps one
                             // phase per use of its stage (the MMA warp does not
                             // wait on it: it waited on the first one)
-                            mbar_arrive_expect_tx(&full[ring.i], 2 * C::kStageBytes);
-                            tma_load_3d(sm_a + ring.i * C::kABytes, &tmap_a2, &full[ring.i], 0, w.a_row0, k);
+                            mbar_arrive_expect_tx(&full[ring.i], 2 * (a_bytes + C::kBBytes));
+                            if (p.a_box_rows == kBM) {
+                                tma_load_3d(sm_a + ring.i * C::kABytes, &tmap_a2, &full[ring.i], 0, w.a_row0, k);
+                            } else {
+                                // a short A box: one 2-D copy per stage (a 3-D box would pack
+                                // the two K blocks' rows together)
+                                tma_load_2d(sm_a + ring.i * C::kABytes, &tmap_a, &full[ring.i], k * kBK, w.a_row0);
+                                tma_load_2d(sm_a + (ring.i + 1) * C::kABytes, &tmap_a, &full[ring.i], (k + 1) * kBK,
+                                            w.a_row0);
+                            }
                             tma_load_3d(sm_b + ring.i * C::kBBytes, &tmap_b2, &full[ring.i], 0, b_row0, k);
                             mbar_arrive(&full[ring.i + 1]);
                             issued |= 2u << ring.i;
                             issued_parity = (issued_parity & ~(2u << ring.i)) | (ring.ph << (ring.i + 1));
                         } else {
                             // when sharing, rank 1's A arrives from rank 0 (same byte count)
-                            mbar_arrive_expect_tx(&full[ring.i], C::kStageBytes);
+                            mbar_arrive_expect_tx(&full[ring.i], a_bytes + C::kBBytes);
                             if (!SHARE || rank == 0)
                                 tma_load_2d(sm_a + ring.i * C::kABytes, &tmap_a, &full[ring.i], k * kBK, w.a_row0);
                             tma_load_2d(sm_b + ring.i * C::kBBytes, &tmap_b, &full[ring.i], k * kBK, b_row0);
@@ -795,7 +804,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                                                   C::kSlotSfbStride * sfb_row) + (sfb_idx0 & 3) + kc;
 
                 const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + acc_ring.i * BN + h * COLS;
-                promote_block<COLS, 64>(acc, taddr, pa, pb, &tempty[acc_ring.i], lane);
+                if (w.valid_rows > 32 * q)
+                    promote_block<COLS, 64>(acc, taddr, pa, pb, &tempty[acc_ring.i], lane);
+                else
+                    release_tmem(&tempty[acc_ring.i], lane);   // rows past M: nothing to read
                 acc_ring.template next<NACC>();
                 ring.template next<S>();
                 if (kc == kScaleChunk - 1 || k + 1 == w.kb1) {

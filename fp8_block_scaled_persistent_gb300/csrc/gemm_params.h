@@ -44,6 +44,10 @@ struct Params {
     int a_rows_total;  // A: rows (masked: G * M_max)
     int b_rows_total;  // B: G * N
     int d_rows_total;  // D: rows (masked: G * M_max)
+    // rows of A each copy brings (128, or 64 for the plain GEMM with M <= 64:
+    // the MMA's rows 64..127 then read whatever the stage holds, and no warp
+    // stores, publishes or reduces them)
+    int a_box_rows;
 };
 
 }  // namespace fp8g
