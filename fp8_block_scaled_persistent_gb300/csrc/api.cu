@@ -190,6 +190,24 @@ bool make_pair_map(CUtensorMap *m, const void *base, uint64_t rows, int K, uint3
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The fp32 addend C [rows][N] viewed as [N/16][rows][16] (slab stride 64
+// bytes), with boxes of 4 slabs x 32 rows, 64-byte swizzled: one copy brings
+// 32 rows x 64 columns of C into one epilogue warp's staging area.
+bool make_c_map(CUtensorMap *m, const float *C, uint64_t rows, int N)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    cuuint64_t dims[3] = {16, rows, (cuuint64_t)(N / 16)};
+    cuuint64_t strides[2] = {(cuuint64_t)N * 4, 64};
+    cuuint32_t box[3] = {16, 32, 4};
+    cuuint32_t es[3] = {1, 1, 1};
+    std::memset(m, 0, sizeof(*m));
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(C), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------ validation
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -479,6 +497,9 @@ int run_nt(const void *A, const float *SFA, const void *B, const float *SFB, con
     }
     if (!make_maps(a, A, SFA, B, SFB, D, M, N, M, a.p.kb, a.p.sfa_ld, (long long)a.p.nb * a.p.kb, N, K,
                    c.block_n))
+        return FP8G_ERR_CUDA;
+    // the accumulate kernel with whole-tile staging copies C by TMA (unsplit)
+    if (C && c.block_n == 256 && !c.split_ctas && !make_c_map(&a.tmap_c, C, (uint64_t)M, N))
         return FP8G_ERR_CUDA;
     a.grid = c.grid;
     a.stream = reinterpret_cast<cudaStream_t>(stream);

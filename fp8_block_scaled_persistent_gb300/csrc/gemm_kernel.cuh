@@ -22,7 +22,13 @@
 //               epilogue the buffer is complete: each commit drains the tensor
 //               pipe, so there is only one.  512 TMEM columns hold 512/BN
 //               buffers, so the MMA of block k+1 runs while k is promoted.
-//   warps 2-3   idle (they only give their registers away).
+//   warp 2      with an fp32 addend and whole-tile staging (accumulate,
+//               256-column tiles, unsplit): the addend/store warp.  One thread
+//               TMA-loads each tile's C into the staging area, half a tile at a
+//               time, and TMA-stores the bf16 tile the epilogue leaves there,
+//               so the epilogue warps neither copy C nor wait for stores.
+//               Otherwise (and warp 3 always) idle: it only gives its
+//               registers away.
 //   warps 4-11  epilogue: tcgen05.ld of the K block's partial, promotion
 //               acc += (sa*sb) * P in fp32 registers (one row per thread,
 //               BN/2 columns per warp), and at the end of a tile bf16
@@ -110,7 +116,7 @@ struct Cfg {
     static constexpr int kPanelBytes = 32 * kPanelCols * 2;
     static constexpr int kPanelsPerWarp = kFullTileStaging ? (BN / 2) / kPanelCols : 2;
     static constexpr int kStagingBytes = kNumEpiWarps * kPanelsPerWarp * kPanelBytes;
-    static constexpr int kBarriers = 2 * kStages + kAccBufs + 2 * kScaleSlots + 1;
+    static constexpr int kBarriers = 2 * kStages + kAccBufs + 2 * kScaleSlots + 1 + 3;
     static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + kScaleSlots * kSlotBytes +
                                       kBarriers * 8 + 16 + 1024 /* alignment slack */;
     static_assert(kSlotTxBytes <= kSlotBytes, "scale slot");
@@ -290,7 +296,7 @@ __device__ __forceinline__ int unit_owner(int v, int U, int P)
 
 // Writes PC columns (one staging panel) of this warp's 32 rows to D.
 // accp holds this thread's row, columns x .. x+PC-1 of the output.
-template <int PC, bool kWaitBuffer>
+template <int PC, bool kWaitBuffer, bool kIssue = true>
 __device__ __forceinline__ void store_panel(const float *accp, uint8_t *panel, const CUtensorMap *tmap_d,
                                             const Params &p, int x, int y_row0, int rows_ok, int lane)
 {
@@ -317,7 +323,7 @@ __device__ __forceinline__ void store_panel(const float *accp, uint8_t *panel, c
             st_shared_v4(base + ((c ^ sw) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
         fence_proxy_async_shared();
         __syncwarp();
-        if (lane == 0) {
+        if (kIssue && lane == 0) {      // (otherwise the addend/store warp issues it)
             tma_store_2d(tmap_d, panel, x, y_row0);
             bulk_commit_group();
         }
@@ -468,6 +474,34 @@ __device__ __forceinline__ void add_c_half(float (&acc)[COLS], const uint8_t *st
     __syncwarp();                       // read by every lane before the next half lands
 }
 
+// The same addition from the addend/store warp's TMA copy of a half: four
+// slabs of 32 rows x 16 fp32 columns (64 bytes a row), 64-byte swizzled
+// (16-byte chunk c of row r at c ^ ((r >> 1) & 3)), so each group of eight
+// lanes reads all 32 banks.  The warp's bf16 rows later overwrite this area,
+// and lane r's row lands on other lanes' C: the closing __syncwarp in the
+// caller orders every lane's reads first.
+template <int COLS>
+__device__ __forceinline__ void add_c_box(float (&acc)[COLS], const uint8_t *stage, int lane, int rd)
+{
+    const uint32_t row = smem_u32(stage) + lane * 64;
+    const int sw = (lane >> 1) & 3;
+#pragma unroll
+    for (int b0 = 0; b0 < 4; b0 += 2) {
+        float4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            v[i] = ld_shared_f4_nc(row + (b0 + (i >> 2)) * 2048 + (((i & 3) ^ sw) << 4));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float *a = acc + rd * kAddendHalfCols + 16 * (b0 + (i >> 2)) + 4 * (i & 3);
+            a[0] += v[i].x;
+            a[1] += v[i].y;
+            a[2] += v[i].z;
+            a[3] += v[i].w;
+        }
+    }
+}
+
 // ----------------------------------------------------------------------------
 // The kernel
 
@@ -486,11 +520,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_sfa,
                     const __grid_constant__ CUtensorMap tmap_sfb, const __grid_constant__ CUtensorMap tmap_a2,
-                    const __grid_constant__ CUtensorMap tmap_b2, const __grid_constant__ Params p)
+                    const __grid_constant__ CUtensorMap tmap_b2, const __grid_constant__ CUtensorMap tmap_c,
+                    const __grid_constant__ Params p)
 {
 #if defined(__CUDA_ARCH__)
     using C = Cfg<BN>;
     static_assert(!SHARE || (!SPLIT && !C::kPairLoads), "A sharing: unsplit schedules, one K block per copy");
+    // the addend/store warp (warp 2): accumulate, whole-tile staging, unsplit
+    constexpr bool kHelperC = KIND == kKindNTAcc && C::kFullTileStaging && !SPLIT;
+    static_assert(!(kHelperC && SHARE), "warp 2 has one role");
     constexpr int S = C::kStages;
     constexpr int NACC = C::kAccBufs;
     constexpr int SR = C::kScaleSlots;
@@ -510,7 +548,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     uint64_t *sfull = tempty + NACC;   // SR: scale slot landed (TMA transactions)
     uint64_t *sempty = sfull + SR;     // SR: epilogue finished reading a scale slot
     uint64_t *drain = sempty + SR;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *c_full = drain + 1;      // a half tile of C landed in the staging area (TMA transactions)
+    uint64_t *c_free = c_full + 1;     // every epilogue warp has added the first half
+    uint64_t *d_ready = c_free + 1;    // every epilogue warp has left its bf16 rows in the staging area
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(d_ready + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -529,6 +570,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_init(&sempty[i], kNumEpiWarps);
         }
         mbar_init(drain, 1);
+        mbar_init(c_full, 1);
+        mbar_init(c_free, kNumEpiWarps);
+        mbar_init(d_ready, kNumEpiWarps);
         *abort_flag = 0;
         fence_mbarrier_init();
         fence_proxy_async_shared();
@@ -543,6 +587,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             prefetch_tensormap(&tmap_a2);
             prefetch_tensormap(&tmap_b2);
         }
+        if (kHelperC)
+            prefetch_tensormap(&tmap_c);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
@@ -682,6 +728,61 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     ring.template next<S>();
                 }
             }
+        } else if (kHelperC && warp == 2 && lane == 0) {
+            // ------------------------------------------------ addend/store (accumulate)
+            // Per tile: once the previous tile's stores have read the staging
+            // area, C's first half (64 of each warp's 128 columns) goes into
+            // it, one 3-D box of 4 x 32 rows x 16 fp32 columns per epilogue
+            // warp; when every warp has added it, the second half; when every
+            // warp has left its bf16 rows there, the tile's stores.  Rows past
+            // M and columns past N arrive as zeros.
+            Scheduler<BN, KIND, SPLIT, SHARE> sched(p, false);
+            Work w;
+            uint32_t ph = 0, c_issued = 0;
+            bool pending = false, ok = true;
+            while (ok && sched.next(w)) {
+                if (pending)
+                    bulk_wait_group_read<0>();
+                const int chunk0 = (w.n_blk * BN) / 16;     // the tile's first 16-column slab of C
+                for (int rd = 0; rd < 2 && ok; ++rd) {
+                    if (rd == 1 && !mbar_wait(c_free, ph, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(c_full, kNumEpiWarps * C::kPanelsPerWarp * C::kPanelBytes);
+#pragma unroll 1
+                    for (int e = 0; e < kNumEpiWarps; ++e)
+                        tma_load_3d(sm_stage_d + e * C::kPanelsPerWarp * C::kPanelBytes, &tmap_c, c_full, 0,
+                                    w.a_row0 + 32 * (e & 3), chunk0 + (e >> 2) * (COLS / 16) + rd * 4);
+                    ++c_issued;
+                }
+                if (!ok || !mbar_wait(d_ready, ph, ctl)) {
+                    ok = false;
+                    break;
+                }
+                ph ^= 1u;
+#pragma unroll 1
+                for (int e = 0; e < kNumEpiWarps; ++e) {
+                    // the epilogue's rule: full 32-row slabs go by TMA, others were
+                    // written by their warp directly
+                    if (w.valid_rows - 32 * (e & 3) < 32)
+                        continue;
+                    for (int pi = 0; pi < COLS / C::kPanelCols; ++pi) {
+                        const int x = w.n_blk * BN + (e >> 2) * COLS + pi * C::kPanelCols;
+                        if (x < p.N)
+                            tma_store_2d(&tmap_d,
+                                         sm_stage_d + e * C::kPanelsPerWarp * C::kPanelBytes + pi * C::kPanelBytes,
+                                         x, w.a_row0 + 32 * (e & 3));
+                    }
+                }
+                bulk_commit_group();
+                pending = true;
+            }
+            // every store is done and the last addend copy has landed before
+            // the CTA exits
+            bulk_wait_group<0>();
+            if (c_issued)
+                mbar_wait_drain(c_full, (c_issued - 1) & 1u, p.timeout_ns);
         } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------ MMA issuer
             Scheduler<BN, KIND, SPLIT, SHARE> sched(p, false);
@@ -747,19 +848,45 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         Work w;
         Ring ring, acc_ring, sring;
         bool ok = true;
+        uint32_t cph = 0;       // phase of c_full this warp waits for next (addend/store warp)
         while (ok && sched.next(w)) {
             float acc[COLS];
             // staged addend (kKindNTAcc, whole-tile staging): the rows this
             // warp adds C to (none unless this CTA stores the tile), and the
             // K blocks after which half 0 is copied and then added (with
             // half 1 copied); short ranges do both halves after the loop
-            constexpr bool kStagedC = KIND == kKindNTAcc && C::kFullTileStaging;
+            constexpr bool kStagedC = KIND == kKindNTAcc && C::kFullTileStaging && !kHelperC;
             static_assert(!kStagedC || (COLS == 2 * kAddendHalfCols &&
                                         C::kPanelsPerWarp * C::kPanelBytes >= 32 * kAddendHalfCols * 4),
                           "addend halves");
             const int c_rows = (kStagedC && w.kb1 == p.kb) ? min(max(w.valid_rows - 32 * q, 0), 32) : 0;
             const bool c_early = w.kb1 - w.kb0 >= 8;
             const int k_copy0 = w.kb0 + 3, k_add0 = w.kb1 - 3;
+            // with the addend/store warp, half 0 is added six K blocks into
+            // the tile (halfway, for shorter ranges): its copy has landed by
+            // then, and the copy of half 1 that this releases has the rest of
+            // the tile to land (adding it three blocks before the end, like
+            // the cp.async path, left the epilogue waiting for half 1: 4096 x
+            // 7168 x 2048 took 81.9 us, against 70.6 us this way)
+            const int k_c0 = w.kb0 + min(6, (w.kb1 - w.kb0) / 2);
+            // with the addend/store warp: wait for half rd of C, add it and,
+            // for the first half, hand the staging area back
+            auto take_c = [&](int rd) -> bool {
+                int got = 1;
+                if (lane == 0)
+                    got = mbar_wait(c_full, cph, ctl) ? 1 : 0;
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got)
+                    return false;
+                cph ^= 1u;
+                __syncwarp();
+                add_c_box<COLS>(acc, panels, lane, rd);
+                __syncwarp();           // every lane's reads before the area is reused
+                if (rd == 0 && lane == 0)
+                    mbar_arrive(c_free);
+                return true;
+            };
+            (void)take_c;
             if (KIND == kKindNTAcc &&
                 !bounds_ok(w.a_row0 + w.valid_rows <= p.rows && w.n_blk * BN < p.N, ctl)) {
                 ok = false;
@@ -817,6 +944,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     if (lane == 0)
                         mbar_arrive(&sempty[sring.i]);
                     sring.template next<SR>();
+                }
+                if constexpr (kHelperC) {
+                    if (c_early && k == k_c0 && !take_c(0)) {
+                        ok = false;
+                        break;
+                    }
                 }
                 if constexpr (kStagedC) {
                     if (c_rows > 0 && c_early && k == k_copy0) {
@@ -916,7 +1049,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int y_row0 = w.a_row0 + 32 * q;
             if (rows_ok > 0 && !bounds_ok(y_row0 >= 0 && y_row0 + rows_ok <= p.d_rows_total, ctl))
                 rows_ok = 0;
-            if constexpr (C::kFullTileStaging) {
+            if constexpr (kHelperC) {
+                // the addend/store warp has waited for the previous tile's
+                // stores; each lane overwrites only its own row of C below
+                if ((!c_early && !take_c(0)) || !take_c(1)) {
+                    ok = false;
+                    break;
+                }
+            } else if constexpr (C::kFullTileStaging) {
                 // the previous tile's stores have had a whole tile to read
                 // this warp's staging area; make sure they are done
                 if (lane == 0)
@@ -941,14 +1081,21 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     continue;
                 // TMA store unless the slab's rows straddle the end of D's rows
                 if constexpr (C::kFullTileStaging) {
-                    store_panel<PC, false>(acc + pi * PC, panels + pi * C::kPanelBytes, &tmap_d, p, x, y_row0,
-                                           rows_ok, lane);
+                    store_panel<PC, false, !kHelperC>(acc + pi * PC, panels + pi * C::kPanelBytes, &tmap_d, p, x,
+                                                      y_row0, rows_ok, lane);
                 } else {
                     uint8_t *buf = panels + (panel_ctr & 1u) * C::kPanelBytes;
                     store_panel<PC, true>(acc + pi * PC, buf, &tmap_d, p, x, y_row0, rows_ok, lane);
                     if (rows_ok == 32)
                         ++panel_ctr;
                 }
+            }
+            if constexpr (kHelperC) {
+                // the full 32-row slabs are in the staging area: the
+                // addend/store warp stores them
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(d_ready);
             }
         }
         if constexpr (KIND == kKindNTAcc)

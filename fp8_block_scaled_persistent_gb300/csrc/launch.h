@@ -15,6 +15,10 @@ struct LaunchArgs {
     // A and B viewed as [K/128][rows][128 B] with boxes two K blocks deep
     // (zeroed, and never used, when K/128 < 2)
     CUtensorMap tmap_a2, tmap_b2;
+    // the fp32 addend C [rows][N] viewed as [N/16][rows][16] with boxes of
+    // 4 x 32 rows x 16 columns, for the accumulate kernel whose addend/store
+    // warp copies it (zeroed, and never used, otherwise)
+    CUtensorMap tmap_c{};
     Params p;
     int grid;
     cudaStream_t stream;

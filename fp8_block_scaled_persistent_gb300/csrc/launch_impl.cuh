@@ -50,7 +50,7 @@ cudaError_t launch_one(const LaunchArgs &a)
     cfg.attrs = attr;
     cfg.numAttrs = SHARE ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, a.tmap_a, a.tmap_b, a.tmap_d, a.tmap_sfa, a.tmap_sfb, a.tmap_a2, a.tmap_b2,
-                              a.p);
+                              a.tmap_c, a.p);
 }
 
 // Clusters of two of the A-sharing instantiation that can be resident at once
