@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfp8gemm.so")
 SOURCES = ["api.cu", "gemm_nt.cu", "gemm_nt_acc.cu", "gemm_contiguous.cu", "gemm_masked.cu",
-           "gemm_pair.cu", "gemm_pair256.cu", "gemm_ue8m0.cu",
+           "gemm_pair.cu", "gemm_pair256.cu", "gemm_ue8m0.cu", "gemm_ue8m0_pair.cu",
            "gemm_share.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

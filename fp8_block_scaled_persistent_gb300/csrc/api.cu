@@ -693,13 +693,17 @@ int fp8_gemm_nt_ue8m0(const void *A, const void *SFA_e, const void *B, const voi
     int st;
     if ((st = current_device_info(dev)) != FP8G_OK)
         return st;
-    const int bn = fp8g::ue8m0_block_n();
+    // CTA pairs (256 x 256 tiles) when asked for with fp8_gemm_set_pair_mode(1)
+    const int mode = g_override_pair.load();
+    const int pairs = mode == 1 ? fp8g::ue8m0_pair_max_active(dev.id) : 0;
+    const bool pair = pairs > 0;
+    const int bn = pair ? fp8g::ue8m0_pair_block_n() : fp8g::ue8m0_block_n();
     LaunchArgs a;
     fill_common(a.p, M, N, K, 1, nullptr, nullptr, D, nullptr, bn, dev);
     a.p.sfa_e = static_cast<const uint8_t *>(SFA_e);
     a.p.sfb_e = static_cast<const uint8_t *>(SFB_e);
-    a.p.num_m_blocks = ceil_div(M, 128);
-    a.p.group_m = 8;
+    a.p.num_m_blocks = ceil_div(M, pair ? 256 : 128);
+    a.p.group_m = pair ? 4 : 8;
     a.p.num_tiles = a.p.num_m_blocks * a.p.num_n_blocks;
     const int pc = fp8g::ue8m0_panel_cols();
     std::memset(&a.tmap_sfa, 0, sizeof(a.tmap_sfa));
@@ -707,12 +711,16 @@ int fp8_gemm_nt_ue8m0(const void *A, const void *SFA_e, const void *B, const voi
     std::memset(&a.tmap_a2, 0, sizeof(a.tmap_a2));
     std::memset(&a.tmap_b2, 0, sizeof(a.tmap_b2));
     if (!make_map(&a.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&a.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, (uint32_t)bn,
+        !make_map(&a.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, (uint32_t)(pair ? bn / 2 : bn),
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&a.tmap_d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, N, M, (uint64_t)N * 2, pc, 32, panel_swizzle(pc)))
         return FP8G_ERR_CUDA;
-    a.grid = std::min(dev.sms, a.p.num_tiles);
     a.stream = reinterpret_cast<cudaStream_t>(stream);
+    if (pair) {
+        a.grid = 2 * std::min(pairs, a.p.num_tiles);
+        return to_status(fp8g::launch_ue8m0_pair(a));
+    }
+    a.grid = std::min(dev.sms, a.p.num_tiles);
     return to_status(fp8g::launch_ue8m0(a));
 }
 

@@ -61,5 +61,12 @@ int max_active_share_pairs(int dev);
 cudaError_t launch_ue8m0(const LaunchArgs &a);
 int ue8m0_block_n();
 int ue8m0_panel_cols();
+// The same on CTA pairs (256 x 256 tiles): tmap_a boxes of 128 rows, tmap_b
+// boxes of ue8m0_pair_block_n() / 2 rows, tmap_d panels of
+// ue8m0_panel_cols() columns; a.grid = 2 x clusters.
+cudaError_t launch_ue8m0_pair(const LaunchArgs &a);
+int ue8m0_pair_block_n();
+// Clusters of two of the pair kernel that can be resident at once (0 on failure).
+int ue8m0_pair_max_active(int dev);
 
 }  // namespace fp8g

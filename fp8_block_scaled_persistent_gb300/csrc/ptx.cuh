@@ -743,6 +743,20 @@ __device__ __forceinline__ void mma_f8f6f4_pair(uint32_t d_tmem, uint64_t a_desc
 // Arrives once on the mbarrier at the same shared-memory offset as `bar` in
 // every CTA of `cta_mask` when the pair MMAs this thread issued so far have
 // completed.
+// The block-scaled MMA across the CTA pair (M = 256): the scale addresses
+// name the same tensor-memory columns in both CTAs.
+__device__ __forceinline__ void mma_mxf8f6f4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_pair(uint64_t *bar, uint16_t cta_mask)
 {
     asm volatile(

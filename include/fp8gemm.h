@@ -216,7 +216,10 @@ int fp8_gemm_set_override(int block_n, int split_ctas);
  *             share one 256 x 128 output tile through tcgen05.mma.cta_group::2
  *             (each CTA loads its own 128 rows of A and half of the tile's B;
  *             nothing is multicast) -- unless a block_n override other than
- *             128 is set;
+ *             128 is set; and every fp8_gemm_nt_ue8m0 call on CTA pairs
+ *             sharing 256 x 256 tiles through the block-scaled
+ *             tcgen05.mma.cta_group::2 (each CTA holds the scales of its own
+ *             rows and of all 256 columns in its tensor memory);
  *   mode  2 : run every unsplit plain, contiguous and masked call (not the
  *             addend variant) with 128 x 256 tiles in clusters of two CTAs
  *             that compute neighbouring n-blocks of one m-block: the first

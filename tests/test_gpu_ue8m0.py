@@ -5,7 +5,8 @@ Element by element on ragged shapes (M and N tails, one and many K blocks,
 K block counts that leave a partial scale chunk), bit for bit on exact
 small-integer inputs with exponents 124..130, the scale-doubling invariant
 (raising one B block's exponent by one doubles exactly that block's columns),
-determinism, and the full-size dense shapes on sampled rows.
+determinism, and the full-size dense shapes on sampled rows; each on the
+one-CTA kernel and on CTA pairs.
 """
 import numpy as np
 import pytest
@@ -18,6 +19,17 @@ from tests.tolerance import check
 pytestmark = pytest.mark.gpu
 
 THREADS = oracle.default_threads()
+
+
+@pytest.fixture(autouse=True, params=[0, 1], ids=["one_cta", "pair"])
+def cta_mode(request):
+    """Every test runs on the one-CTA kernel (128 x 256 tiles) and on CTA
+    pairs (256 x 256 tiles, fp8_gemm_set_pair_mode(1))."""
+    import fp8_block_scaled_persistent_gb300 as fg
+    assert fg.fp8_gemm_set_pair_mode(request.param) == fg.FP8G_OK
+    yield request.param
+    fg.fp8_gemm_set_pair_mode(0)
+    assert fg.fp8_gemm_get_device_error() == 0
 
 
 def _ref(p, rows=None):
