@@ -228,7 +228,8 @@ int fp8_gemm_set_override(int block_n, int split_ctas);
  *             reads A from global memory once.  A block_n override other than
  *             256 turns it off.  Source: TVM TIRx, the "copy_async -> dsmem"
  *             two-CTA shared-to-shared bulk copy;
- *   mode  0 : the automatic choice (the default);
+ *   mode  0 : the automatic choice (the default): one CTA per tile, except
+ *             fp8_gemm_nt_ue8m0 with M > 128, which runs on CTA pairs;
  *   mode -1 : never use CTA pairs.
  * Results are the same to within fp32 rounding order (bit-identical on
  * exactly representable inputs).  Returns FP8G_ERR_INVALID_ARG for other

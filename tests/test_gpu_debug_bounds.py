@@ -85,8 +85,11 @@ for mode, bn in ((1, 128), (1, 256), (2, 256)):
     run(wl.make_masked([5, 200, 0, 256], 256, 528, 256, seed=9), f"mode{mode} bn{bn} masked")
 fg.fp8_gemm_set_pair_mode(0)
 fg.fp8_gemm_set_override(0, 0)
-for M, N, K in [(63, 48, 256), (300, 528, 2304)]:
-    run(wl.make_nt_ue8m0(M, N, K, seed=M), f"ue8m0 {M}x{N}x{K}")
+for mode in (-1, 1):
+    fg.fp8_gemm_set_pair_mode(mode)
+    for M, N, K in [(63, 48, 256), (300, 528, 2304)]:
+        run(wl.make_nt_ue8m0(M, N, K, seed=M), f"ue8m0 mode{mode} {M}x{N}x{K}")
+fg.fp8_gemm_set_pair_mode(0)
 torch.cuda.synchronize()
 print("debug build ok", cases)
 '''

@@ -21,10 +21,11 @@ pytestmark = pytest.mark.gpu
 THREADS = oracle.default_threads()
 
 
-@pytest.fixture(autouse=True, params=[0, 1], ids=["one_cta", "pair"])
+@pytest.fixture(autouse=True, params=[-1, 1], ids=["one_cta", "pair"])
 def cta_mode(request):
-    """Every test runs on the one-CTA kernel (128 x 256 tiles) and on CTA
-    pairs (256 x 256 tiles, fp8_gemm_set_pair_mode(1))."""
+    """Every test runs on the one-CTA kernel (128 x 256 tiles,
+    fp8_gemm_set_pair_mode(-1)) and on CTA pairs (256 x 256 tiles,
+    fp8_gemm_set_pair_mode(1))."""
     import fp8_block_scaled_persistent_gb300 as fg
     assert fg.fp8_gemm_set_pair_mode(request.param) == fg.FP8G_OK
     yield request.param
