@@ -897,6 +897,7 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const float *SFA, const void *
 
     LaunchArgs a;
     fill_common(a.p, M, N, K, 1, SFA, SFB, D, nullptr, c.block_n, dev);
+    a.p.a_box_rows = M <= 64 ? 64 : 128;    // as fp8_gemm_nt
     a.p.num_m_blocks = ceil_div(M, 128);
     a.p.group_m = 8;
     a.p.num_tiles = c.tiles;
