@@ -195,8 +195,10 @@ def fp8_gemm_set_override(block_n=0, split_ctas=0) -> int:
 
 
 def fp8_gemm_set_pair_mode(mode=0) -> int:
-    """1: unsplit calls run on CTA pairs (256 x 128 tiles over two SMs),
-    0: automatic choice, -1: never.  Returns the status code."""
+    """1: unsplit calls run on CTA pairs (256 x 128 tiles over two SMs; the
+    power-of-two-scale GEMM on 256 x 256 tiles), 2: A-sharing clusters,
+    0: automatic choice (pairs only for the power-of-two-scale GEMM with
+    M > 128), -1: never.  Returns the status code."""
     return library().fp8_gemm_set_pair_mode(int(mode))
 
 
