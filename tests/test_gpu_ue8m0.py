@@ -5,8 +5,8 @@ Element by element on ragged shapes (M and N tails, one and many K blocks,
 K block counts that leave a partial scale chunk), bit for bit on exact
 small-integer inputs with exponents 124..130, the scale-doubling invariant
 (raising one B block's exponent by one doubles exactly that block's columns),
-determinism, and the full-size dense shapes on sampled rows; each on the
-one-CTA kernel and on CTA pairs.
+determinism, a CUDA graph replay, and the full-size dense shapes on sampled
+rows; each on the one-CTA kernel and on CTA pairs.
 """
 import numpy as np
 import pytest
@@ -93,6 +93,37 @@ def test_ue8m0_deterministic():
     a, _, _ = gu.run(p)
     b, _, _ = gu.run(p)
     assert np.array_equal(a, b)
+
+
+def test_ue8m0_graph_replay_bit_identical():
+    """Two shapes captured into one CUDA graph on a side stream replay, twice,
+    to the eager calls' bits (the pair path launches clusters of two)."""
+    import torch
+    import fp8_block_scaled_persistent_gb300 as fg
+    probs = [wl.make_nt_ue8m0(300, 528, 2304, seed=6), wl.make_nt_ue8m0(64, 256, 512, seed=7)]
+    tens = [gu.dev_tensors(p) for p in probs]
+    side = torch.cuda.Stream()
+    ref = [gu.new_d(p) for p in probs]
+    with torch.cuda.stream(side):
+        for p, t, D in zip(probs, tens, ref):
+            assert gu.call(p, t, D, stream=side) == 0
+    side.synchronize()
+    assert fg.fp8_gemm_get_device_error(side) == 0
+    ref_bits = [gu.bits(D) for D in ref]
+    outs = [gu.new_d(p) for p in probs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for p, t, D in zip(probs, tens, outs):
+            assert gu.call(p, t, D, stream=side) == 0
+    for _ in range(2):
+        for D in outs:
+            D.view(torch.int16).fill_(np.int16(np.uint16(gu.SENTINEL).view(np.int16)))
+        g.replay()
+        torch.cuda.synchronize()
+        assert fg.fp8_gemm_get_device_error() == 0
+        for i, (D, r) in enumerate(zip(outs, ref_bits)):
+            assert np.array_equal(gu.bits(D), r), f"replay output {i}"
+    check(ref_bits[0], _ref(probs[0]), "ue8m0 graph 300x528x2304")
 
 
 def test_ue8m0_argument_checks():
