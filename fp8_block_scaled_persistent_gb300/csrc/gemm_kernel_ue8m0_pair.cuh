@@ -202,11 +202,14 @@ __global__ void __launch_bounds__(Ue8m0PairCfg::kThreads, 1)
                 }
                 const int n = min(C::kChunk, p.kb - k0);
                 const uint32_t slot = tmem_base + C::kScaleCol0 + sring.i * C::kChunk * C::kSlotCols;
-                for (int kc = 0; kc < n; ++kc) {
+                // one K block: its operands, four MMAs, the commit that frees
+                // the stage; a whole chunk runs fully unrolled (no loop
+                // branch per K block on the issuing thread: 42.2 -> 41.6 us at
+                // 4096 x 7168 x 2048)
+                auto kblock = [&](int kc) -> bool {
                     const int k = k0 + kc;
                     if (!mbar_wait(&full[ring.i], ring.ph, ctl)) {
-                        ok = false;
-                        break;
+                        return false;
                     }
                     tc_fence_after_sync();
                     const uint64_t a0 = sdesc_kmajor_sw128(smem_u32(sm_a + ring.i * C::kABytes));
@@ -219,6 +222,21 @@ __global__ void __launch_bounds__(Ue8m0PairCfg::kThreads, 1)
                                           (k | kk) != 0 ? 1u : 0u);
                     mma_commit_pair(&empty[ring.i], 0x3);
                     ring.template next<S>();
+                    return true;
+                };
+                if (n == C::kChunk) {
+#pragma unroll
+                    for (int kc = 0; kc < C::kChunk; ++kc)
+                        if (!kblock(kc)) {
+                            ok = false;
+                            break;
+                        }
+                } else {
+                    for (int kc = 0; kc < n; ++kc)
+                        if (!kblock(kc)) {
+                            ok = false;
+                            break;
+                        }
                 }
                 if (!ok)
                     break;
