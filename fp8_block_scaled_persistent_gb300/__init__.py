@@ -40,7 +40,8 @@ EXPORTS = (
     "fp8_gemm_nt", "fp8_gemm_nt_accumulate", "fp8_gemm_nt_ue8m0", "fp8_gemm_grouped_contiguous",
     "fp8_gemm_grouped_masked",
     "fp8_gemm_workspace_size", "fp8_gemm_get_device_error", "fp8_gemm_status_string",
-    "fp8_gemm_sfa_ld", "fp8_gemm_set_override", "fp8_gemm_set_pair_mode", "fp8_gemm_workspace_size_for",
+    "fp8_gemm_sfa_ld", "fp8_gemm_set_override", "fp8_gemm_set_pair_mode", "fp8_gemm_set_narrow_mode",
+    "fp8_gemm_workspace_size_for",
     "fp8_gemm_set_wait_timeout_ns", "fp8_gemm_nt_noalloc", "fp8_gemm_version",
 )
 
@@ -91,6 +92,8 @@ def library(path: str | None = None):
         lib.fp8_gemm_set_override.restype = i
         lib.fp8_gemm_set_pair_mode.argtypes = [i]
         lib.fp8_gemm_set_pair_mode.restype = i
+        lib.fp8_gemm_set_narrow_mode.argtypes = [i]
+        lib.fp8_gemm_set_narrow_mode.restype = i
         lib.fp8_gemm_set_wait_timeout_ns.argtypes = [u64]
         lib.fp8_gemm_set_wait_timeout_ns.restype = i
         lib.fp8_gemm_nt_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
@@ -200,6 +203,13 @@ def fp8_gemm_set_pair_mode(mode=0) -> int:
     0: automatic choice (pairs only for the power-of-two-scale GEMM with
     M > 128), -1: never.  Returns the status code."""
     return library().fp8_gemm_set_pair_mode(int(mode))
+
+
+def fp8_gemm_set_narrow_mode(mode=0) -> int:
+    """1: every plain GEMM with M <= 128 runs on the narrow-slice kernel (one
+    CTA per 64-column slice, whole K, no split), 0: automatic choice, -1:
+    never.  Returns the status code."""
+    return library().fp8_gemm_set_narrow_mode(int(mode))
 
 
 def fp8_gemm_set_wait_timeout_ns(ns) -> int:

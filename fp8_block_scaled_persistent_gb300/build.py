@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfp8gemm.so")
 SOURCES = ["api.cu", "gemm_nt.cu", "gemm_nt_acc.cu", "gemm_contiguous.cu", "gemm_masked.cu",
            "gemm_pair.cu", "gemm_pair256.cu", "gemm_ue8m0.cu", "gemm_ue8m0_pair.cu",
-           "gemm_share.cu"]
+           "gemm_share.cu", "gemm_narrow.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

@@ -85,6 +85,25 @@ struct EnvPairMode {
             g_override_pair.store(2);
     }
 } g_env_pair_mode;
+
+// The narrow-slice kernel (plain GEMM, M <= 128): 0 = automatic choice,
+// 1 = wherever it applies, -1 = never.  FP8G_NARROW_MODE="-1" | "0" | "1" sets
+// it when the library loads (anything else is ignored).
+std::atomic<int> g_narrow_mode{0};
+struct EnvNarrowMode {
+    EnvNarrowMode()
+    {
+        const char *v = std::getenv("FP8G_NARROW_MODE");
+        if (!v)
+            return;
+        if (!std::strcmp(v, "-1"))
+            g_narrow_mode.store(-1);
+        else if (!std::strcmp(v, "0"))
+            g_narrow_mode.store(0);
+        else if (!std::strcmp(v, "1"))
+            g_narrow_mode.store(1);
+    }
+} g_env_narrow_mode;
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 
 // ------------------------------------------------------------ device facts
@@ -173,21 +192,28 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t
 }
 
 // An e4m3 operand [rows][K] viewed as [K/128][rows][128 B] (K-block stride
-// 128 bytes), with boxes of box_rows rows x 2 K blocks: one copy fills two
-// consecutive 128-byte-swizzled K-block tiles.
-bool make_pair_map(CUtensorMap *m, const void *base, uint64_t rows, int K, uint32_t box_rows)
+// 128 bytes), with boxes of box_rows rows x `depth` K blocks: one copy fills
+// `depth` consecutive 128-byte-swizzled K-block tiles (K blocks past the end
+// arrive as zeros).
+bool make_kblock_map(CUtensorMap *m, const void *base, uint64_t rows, int K, uint32_t box_rows, uint32_t depth)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc)
         return false;
     cuuint64_t dims[3] = {128, rows, (cuuint64_t)(K / 128)};
     cuuint64_t strides[2] = {(cuuint64_t)K, 128};
-    cuuint32_t box[3] = {128, box_rows, 2};
+    cuuint32_t box[3] = {128, box_rows, depth};
     cuuint32_t es[3] = {1, 1, 1};
     std::memset(m, 0, sizeof(*m));
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Two K blocks per box (the one-CTA kernel's paired stages).
+bool make_pair_map(CUtensorMap *m, const void *base, uint64_t rows, int K, uint32_t box_rows)
+{
+    return make_kblock_map(m, base, rows, K, box_rows, 2);
 }
 
 // The fp32 addend C [rows][N] viewed as [N/16][rows][16] (slab stride 64
@@ -254,20 +280,49 @@ struct NtChoice {
     int split_ctas;   // 0: not split
     int grid;
     int tiles;
+    bool narrow = false;   // the narrow-slice kernel (block_n = its slice width)
 };
+
+// Whether the narrow-slice kernel runs a plain GEMM (no addend) of M x N x K
+// on `sms` SMs: asked for (fp8_gemm_set_narrow_mode(1)) with M <= 128 and at
+// least 4 K blocks (its copies are up to 4 K blocks deep), or, automatically,
+// when M <= 64, there are at least 8 K blocks and its slices keep at least
+// half the SMs busy without needing a second round.  (With 65..128 rows every
+// CTA reading all of A over the whole K range was measured slower than the
+// split-K schedule: 128 x 7168 x 16384, 32.6 against 32.2 us.)  A forced tile
+// width or split rules it out.
+bool want_narrow(int M, int N, int K, int sms)
+{
+    const int mode = g_narrow_mode.load();
+    if (mode < 0 || M > 128 || K / 128 < 4 || g_override_bn.load() != 0 || g_override_split.load() > 0)
+        return false;
+    if (mode > 0)
+        return true;
+    const int slices = ceil_div(N, fp8g::narrow_block_n(M <= 64 ? 64 : 128));
+    return M <= 64 && 2 * slices >= sms && slices <= sms && K / 128 >= 8;
+}
 
 // Tile shape and schedule for a plain GEMM on a device with `sms` SMs.
 // workspace_bytes < 0 means "as much as it needs".  With fewer output tiles
 // than SMs the K blocks of all tiles are shared evenly over the SMs (split-K)
 // with 128-column tiles (6 operand stages keep more of B in flight than the 3
 // of 256-column tiles; measured faster on small-M shapes), else 256-column
-// ones, whichever workspace fits first.
-int choose_nt(int M, int N, int K, int sms, long long workspace_bytes, NtChoice &c)
+// ones, whichever workspace fits first.  With allow_narrow (no addend) small
+// M may go to the narrow-slice kernel instead (want_narrow).
+int choose_nt(int M, int N, int K, int sms, long long workspace_bytes, NtChoice &c, bool allow_narrow = false)
 {
     const int mb = ceil_div(M, 128);
     const int kb = K / 128;
     const int obn = g_override_bn.load();
     const int osplit = g_override_split.load();
+    if (allow_narrow && want_narrow(M, N, K, sms)) {
+        c.narrow = true;
+        c.block_n = fp8g::narrow_block_n(M <= 64 ? 64 : 128);
+        c.split_ctas = 0;
+        c.tiles = ceil_div(N, c.block_n);
+        c.grid = std::min(sms, c.tiles);
+        return FP8G_OK;
+    }
     auto tiles_for = [&](int bn) { return mb * ceil_div(N, bn); };
     // the kernel's split arithmetic is 32-bit: units * CTAs must stay below 2^31
     auto fits32 = [&](int bn, long long P) { return (long long)tiles_for(bn) * kb * P < (1ll << 31); };
@@ -462,6 +517,31 @@ int run_nt_pair(const void *A, const float *SFA, const void *B, const float *SFB
     return to_status(fp8g::launch_pair(C ? fp8g::kKindNTAcc : fp8g::kKindNT, bn, a));
 }
 
+// The plain GEMM (M <= 128, no addend) on the narrow-slice kernel.
+int run_nt_narrow(const void *A, const float *SFA, const void *B, const float *SFB, void *D, int M, int N, int K,
+                  const NtChoice &c, const DeviceInfo &dev, fp8g_stream_t stream)
+{
+    LaunchArgs a;
+    fill_common(a.p, M, N, K, 1, SFA, SFB, D, nullptr, c.block_n, dev);
+    a.p.a_box_rows = M <= 64 ? 64 : 128;    // rows past M are never stored: load only the first 64
+    a.p.num_m_blocks = 1;
+    a.p.num_tiles = c.tiles;
+    const uint32_t kd = (uint32_t)fp8g::narrow_kd(a.p.a_box_rows);
+    std::memset(&a.tmap_d, 0, sizeof(a.tmap_d));
+    std::memset(&a.tmap_a2, 0, sizeof(a.tmap_a2));
+    std::memset(&a.tmap_b2, 0, sizeof(a.tmap_b2));
+    if (!make_kblock_map(&a.tmap_a, A, (uint64_t)M, K, (uint32_t)a.p.a_box_rows, kd) ||
+        !make_kblock_map(&a.tmap_b, B, (uint64_t)N, K, (uint32_t)c.block_n, kd) ||
+        !make_map(&a.tmap_sfa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SFA, a.p.sfa_ld, a.p.kb, (uint64_t)a.p.sfa_ld * 4,
+                  128, fp8g::kScaleChunk, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&a.tmap_sfb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SFB, (uint64_t)a.p.nb * a.p.kb, 0, 0,
+                  fp8g::kScaleChunk + 4, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return FP8G_ERR_CUDA;
+    a.grid = c.grid;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    return to_status(fp8g::launch_narrow(a));
+}
+
 // The plain GEMM, with or without the fp32 addend C (validated by the caller).
 int run_nt(const void *A, const float *SFA, const void *B, const float *SFB, const float *C, void *D, int M, int N,
            int K, void *workspace, size_t workspace_bytes, fp8g_stream_t stream)
@@ -472,8 +552,10 @@ int run_nt(const void *A, const float *SFA, const void *B, const float *SFB, con
         return st;
     NtChoice c;
     const long long ws = workspace ? (long long)workspace_bytes : 0;
-    if ((st = choose_nt(M, N, K, dev.sms, ws, c)) != FP8G_OK)
+    if ((st = choose_nt(M, N, K, dev.sms, ws, c, C == nullptr)) != FP8G_OK)
         return st;
+    if (c.narrow)
+        return run_nt_narrow(A, SFA, B, SFB, D, M, N, K, c, dev, stream);
     if (c.split_ctas && !aligned(workspace, 256))
         return FP8G_ERR_MISALIGNED;
     int pairs = 0;
@@ -808,6 +890,14 @@ int fp8_gemm_set_pair_mode(int mode)
     return FP8G_OK;
 }
 
+int fp8_gemm_set_narrow_mode(int mode)
+{
+    if (mode < -1 || mode > 1)
+        return FP8G_ERR_INVALID_ARG;
+    g_narrow_mode.store(mode);
+    return FP8G_OK;
+}
+
 int fp8_gemm_set_wait_timeout_ns(uint64_t ns)
 {
     if (ns < 1000000ull)
@@ -880,8 +970,10 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const float *SFA, const void *
     // for, or, when that needs more than the static scratch, the best one
     // that fits it; a forced split that does not fit is refused
     NtChoice c;
-    if ((st = choose_nt(M, N, K, dev.sms, -1, c)) != FP8G_OK)
+    if ((st = choose_nt(M, N, K, dev.sms, -1, c, true)) != FP8G_OK)
         return st;
+    if (c.narrow)
+        return run_nt_narrow(A, SFA, B, SFB, D, M, N, K, c, dev, stream);
     if (c.split_ctas && split_workspace_bytes(M, N, K, c.block_n, c.split_ctas) > kNoAllocScratchBytes) {
         if (g_override_split.load() > 0)
             return FP8G_ERR_SCRATCH_LIMIT;

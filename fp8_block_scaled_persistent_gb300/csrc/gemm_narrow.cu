@@ -1,0 +1,80 @@
+// gemm_narrow.cu -- launch of the narrow-slice kernel (gemm_kernel_narrow.cuh)
+// for the plain GEMM with M <= 128: one CTA per slice of narrow_block_n()
+// columns (the grid is min(slices, SMs); a CTA takes slices c, c + grid, ...),
+// 192 threads, programmatic stream serialisation.
+#include <atomic>
+
+#include "gemm_kernel_narrow.cuh"
+
+#ifndef FP8G_PDL
+#define FP8G_PDL 1
+#endif
+// slice width and K blocks per copy, per A box height (64 rows: M <= 64)
+#ifndef FP8G_NARROW64_BN
+#define FP8G_NARROW64_BN 64
+#endif
+#ifndef FP8G_NARROW64_KD
+#define FP8G_NARROW64_KD 4
+#endif
+#ifndef FP8G_NARROW128_BN
+#define FP8G_NARROW128_BN 64
+#endif
+#ifndef FP8G_NARROW128_KD
+#define FP8G_NARROW128_KD 2
+#endif
+#include "launch.h"
+
+namespace fp8g {
+
+namespace {
+
+// as many stages as 192 KB of operands hold
+constexpr int stages_for(int bn, int a_rows, int kd) { return (192 * 1024) / (kd * (a_rows + bn) * kBK); }
+
+template <int BN, int A_ROWS, int KD>
+cudaError_t launch_narrow_one(const LaunchArgs &a)
+{
+    constexpr int S = stages_for(BN, A_ROWS, KD);
+    using C = NarrowCfg<BN, A_ROWS, KD, S>;
+    auto kern = fp8_gemm_narrow_kernel<BN, A_ROWS, KD, S>;
+    static std::atomic<unsigned long long> attr_done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess)
+            return e;
+        attr_done.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.grid, 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = FP8G_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a.tmap_a, a.tmap_b, a.tmap_sfa, a.tmap_sfb, a.p);
+}
+
+}  // namespace
+
+int narrow_block_n(int a_box_rows) { return a_box_rows == 64 ? FP8G_NARROW64_BN : FP8G_NARROW128_BN; }
+
+int narrow_kd(int a_box_rows) { return a_box_rows == 64 ? FP8G_NARROW64_KD : FP8G_NARROW128_KD; }
+
+cudaError_t launch_narrow(const LaunchArgs &a)
+{
+    if (a.p.a_box_rows == 64)
+        return launch_narrow_one<FP8G_NARROW64_BN, 64, FP8G_NARROW64_KD>(a);
+    if (a.p.a_box_rows == 128)
+        return launch_narrow_one<FP8G_NARROW128_BN, 128, FP8G_NARROW128_KD>(a);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fp8g

@@ -97,6 +97,10 @@ def test_overrides_and_timeout_validation(lib):
     assert fg.fp8_gemm_set_override(256, 4) == fg.FP8G_OK
     assert fg.fp8_gemm_set_override(128, 4) == fg.FP8G_OK
     assert fg.fp8_gemm_set_override(0, 0) == fg.FP8G_OK
+    for bad in (-2, 2, 64):
+        assert fg.fp8_gemm_set_narrow_mode(bad) == fg.FP8G_ERR_INVALID_ARG
+    for good in (-1, 1, 0):
+        assert fg.fp8_gemm_set_narrow_mode(good) == fg.FP8G_OK
     assert fg.fp8_gemm_set_wait_timeout_ns(10) == fg.FP8G_ERR_INVALID_ARG
     assert fg.fp8_gemm_set_wait_timeout_ns(2_000_000_000) == fg.FP8G_OK
 

@@ -6,7 +6,8 @@ In that build each kernel checks the invariants its memory accesses rely on
 counter indices are in range; every store stays inside D) and records
 FP8G_ERR_BOUNDS, skipping the access, when one fails.  The cases below run
 in a child process that loads the checking build (FP8G_LIBRARY=debug): the
-plain GEMM at both tile widths with ragged M and N, split-K, the addend,
+plain GEMM at both tile widths with ragged M and N, split-K, the
+narrow-slice kernel (both A box heights, more slices than SMs), the addend,
 both grouped layouts with skipped blocks and short groups, the CTA-pair and
 A-sharing modes, and the power-of-two-scale entry point.  Every result must
 match the oracle and the device error must stay FP8G_OK.
@@ -70,8 +71,13 @@ for bn in (128, 256):
     for M, N, K in shapes:
         run(wl.make_nt(M, N, K, seed=M + N), f"plain bn{bn} {M}x{N}x{K}")
 fg.fp8_gemm_set_override(0, 0)
+fg.fp8_gemm_set_narrow_mode(-1)
 for M, N, K in [(64, 1024, 8192), (100, 384, 1536), (1, 128, 512)]:
     run(wl.make_nt(M, N, K, seed=K), f"split {M}x{N}x{K}")
+fg.fp8_gemm_set_narrow_mode(1)
+for M, N, K in [(1, 16, 512), (63, 336, 2560), (100, 400, 2688), (128, 64 * 160, 512)]:
+    run(wl.make_nt(M, N, K, seed=K + 1), f"narrow {M}x{N}x{K}")
+fg.fp8_gemm_set_narrow_mode(0)
 run(wl.make_nt_acc(130, 272, 640, seed=3), "addend")
 c = wl.make_contiguous([128, 256, 128, 384], 272, 512, seed=21)
 c.m_indices[128:256] = -1

@@ -16,12 +16,16 @@ from tests import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name,reps", [
-    ("smallm_128x7168x16384", 16), ("smallm_64x7168x16384", 16),
-    ("acc_4096x7168x2048", 8), ("masked_g16_m256_n7168_k2048", 8)])
-def test_repeated_launches_bit_identical(name, reps):
+@pytest.mark.parametrize("name,reps,narrow", [
+    ("smallm_128x7168x16384", 16, -1), ("smallm_64x7168x16384", 16, -1),
+    ("smallm_128x7168x16384", 16, 1), ("smallm_64x7168x16384", 16, 1),
+    ("acc_4096x7168x2048", 8, 0), ("masked_g16_m256_n7168_k2048", 8, 0)])
+def test_repeated_launches_bit_identical(name, reps, narrow):
+    """narrow = -1 keeps the small-M shapes on the split-K schedule, 1 puts
+    them on the narrow-slice kernel."""
     import torch
     import fp8_block_scaled_persistent_gb300 as fg
+    assert fg.fp8_gemm_set_narrow_mode(narrow) == fg.FP8G_OK
     p = wl.make(name)
     t = gu.dev_tensors(p)
     ws = gu.workspace_for(p)
@@ -38,3 +42,4 @@ def test_repeated_launches_bit_identical(name, reps):
         # the counters (8 per 128-column tile) lead the workspace
         tiles = ((p.M + 127) // 128) * ((p.N + 127) // 128)
         assert int(ws[: tiles * 8 * 4].view(torch.int32).abs().sum()) == 0
+    fg.fp8_gemm_set_narrow_mode(0)

@@ -25,10 +25,15 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(autouse=True)
 def _reset():
+    # the split-K schedule throughout (the scratch array is what these tests
+    # exercise); the narrow-slice kernel's own no-alloc case is in
+    # test_gpu_narrow.py
     import fp8_block_scaled_persistent_gb300 as fg
     fg.fp8_gemm_set_override(0, 0)
+    fg.fp8_gemm_set_narrow_mode(-1)
     yield
     fg.fp8_gemm_set_override(0, 0)
+    fg.fp8_gemm_set_narrow_mode(0)
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 7168, 16384), (64, 1024, 4096), (300, 512, 1024)])
