@@ -1,23 +1,34 @@
 // gemm_kernel_narrow.cuh -- the plain FP8 (E4M3) GEMM for at most 128 rows of
-// A: one CTA per narrow column slice of the output (48 or 64 columns), the
-// whole K range each, no split and so no partial sums to publish or reduce.
+// A: one CTA per narrow column slice of the output (48, 64 or 96 columns),
+// over the whole K range or over one of two K parts.
 //
 // What is computed: the method's GEMM (DeepGEMM fp8_gemm.cuh, fp8_gemm_kernel:
 // each 128-wide K block's partial product is formed on its own in fp32 and
 // promoted into an fp32 accumulator with scale_a(row, k) * scale_b(n/128, k),
-// rounded to bf16 at the end), in the same K order as the one-CTA kernel.
+// rounded to bf16 at the end).
 //
 // Why a kernel of its own: with M <= 128 the work is one stream of B from
-// HBM.  Split over K (the one-CTA kernel's stream-K schedule), every CTA whose
-// K range ends inside a tile publishes an fp32 partial and another reduces it,
+// HBM.  Split over K the one-CTA kernel's way (stream-K), every CTA whose K
+// range ends inside a tile publishes an fp32 partial and another reduces it,
 // and those partials' trips through the memory system set the tail of the
-// launch.  Here each CTA streams B[BN slice rows][K] once (BN = 48 or 64) and
-// stores its outputs itself.  A 48-column slice may straddle one boundary of
-// the 128-column scale blocks: its scale slots then hold both blocks' B
-// scales and each 16-column chunk of the slice takes its block's.  The narrow
-// tile makes each K block small (6 or 8 KB of B), so the per-K-block costs
-// are batched: every copy brings KD consecutive K blocks (one 3-D box of A,
-// one of B), and the MMA issuer, the epilogue and the buffer releases work a
+// launch.  Here the work units are (slice, K part) pairs, KSPLIT parts per
+// slice, and every CTA's range lies inside one slice:
+//   KSPLIT = 1  each CTA streams B[BN slice rows][K] once and stores its
+//               outputs itself (nothing published);
+//   KSPLIT = 2  the two CTAs of a slice stream one K half each (half of A per
+//               CTA: with 128 rows of A, A's copies rival B's), then trade
+//               halves of the slice: each publishes the fp32 partial of the
+//               columns the other finalises, waits for the other's, adds it
+//               (P0 + P1: fp32 addition commutes, so both orders give the
+//               same bits) and stores its half.  All CTAs of the grid are
+//               resident (one per SM) and every CTA publishes before it
+//               waits, so the waits end.
+// A slice whose width does not divide 128 may straddle one boundary of the
+// 128-column scale blocks: its scale slots then hold both blocks' B scales
+// and each 16-column chunk of the slice takes its block's.  The narrow tile
+// makes each K block small (6 to 12 KB of B), so the per-K-block costs are
+// batched: every copy brings KD consecutive K blocks (one 3-D box of A, one
+// of B), and the MMA issuer, the epilogue and the buffer releases work a
 // whole copy (a "group" of KD K blocks) at a time.
 //
 // 192 threads (six warps):
@@ -28,15 +39,15 @@
 //               scale ring.
 //   warp 1      MMA issuer (and tensor-memory owner): per group, 4 x
 //               tcgen05.mma kind::f8f6f4 (128 x BN x 32) per K block, each K
-//               block into its own 64-column buffer of the group, then one
-//               commit, which frees the stage and tells the epilogue the group
-//               is complete.  512 columns hold 512 / (64 KD) groups.
+//               block into its own buffer of the group, then one commit,
+//               which frees the stage and tells the epilogue the group is
+//               complete.
 //   warps 2-5   epilogue, one per tensor-memory lane quarter (warp & 3): per
-//               K block a tcgen05.ld of its 32 rows x BN columns and
+//               K block tcgen05.ld of its 32 rows x BN columns and
 //               acc += (sa*sb) * P in fp32 registers; the group is released
-//               once its last load has landed.  At the end of a slice, bf16
-//               (round to nearest even) row stores; rows past M and columns
-//               past N are not written.
+//               once its last load has landed.  At the end of a unit, the
+//               trade of halves (KSPLIT = 2) and bf16 (round to nearest even)
+//               row stores; rows past M and columns past N are not written.
 // With A_ROWS = 64 (M <= 64) only the first 64 rows of A are loaded: the MMA
 // still forms 128 rows, whose upper half reads the stage's next bytes (in
 // bounds: B follows A in every stage) and is never read back.
@@ -49,13 +60,14 @@
 
 namespace fp8g {
 
-template <int BN, int A_ROWS, int KD, int S>
+template <int BN, int A_ROWS, int KD, int S, int KSPLIT>
 struct NarrowCfg {
-    static_assert(BN == 48 || BN == 64, "slice width");
+    static_assert(BN == 48 || BN == 64 || BN == 96, "slice width");
+    static_assert(KSPLIT == 1 || (KSPLIT == 2 && BN % 32 == 0), "K parts (a traded half is whole float4s)");
     static_assert(A_ROWS == 64 || A_ROWS == 128, "A box rows");
     static_assert(KD == 2 || KD == 4, "K blocks per copy (a divisor of kScaleChunk)");
     static constexpr int kBN = BN;                          // output columns (B rows) per CTA
-    static constexpr int kBufCols = 64;                     // tensor-memory columns per K block
+    static constexpr int kBufCols = BN <= 64 ? 64 : 128;    // tensor-memory columns per K block
     // 128-column scale blocks a slice can touch
     static constexpr int kSfbRows = (128 % BN == 0) ? 1 : 2;
     static constexpr int kThreads = 192;
@@ -82,39 +94,98 @@ struct NarrowCfg {
     // the epilogue's wait on a stage's MMA completion must not alias: the
     // stage's next use needs the group this warp releases first
     static_assert(S >= kGroups, "stages >= tensor-memory groups");
+    static_assert(kGroups >= 2, "the MMA fills one group while the epilogue reads another");
+    // the two column pieces of one K block's partial (tcgen05.ld of 16, 32 or
+    // 64 columns each)
+    static constexpr int kPiece0 = BN >= 64 ? 64 : 32;
+    static constexpr int kPiece1 = BN - kPiece0;
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
-// This thread's row of one K block's partial: BN columns from taddr on.
-template <int BN>
-__device__ __forceinline__ void narrow_ld(uint32_t taddr, uint32_t (&v)[BN])
+// acc[c] += (c < jb ? s0 : s1) * v[c - C0] for the 16-column chunks of one
+// piece of a K block's partial (columns C0 .. C0 + NV of the slice).
+template <int C0, int NV, int BN>
+__device__ __forceinline__ void promote_piece(float (&acc)[BN], const uint32_t (&v)[NV], int jb, float s0, float s1)
 {
-    if constexpr (BN == 64) {
-        tmem_ld_32x32b_x64(taddr, v);
-        tmem_wait_ld(v);
-    } else {
-        uint32_t v0[32], v1[16];
-        tmem_ld_32x32b_x32(taddr, v0);
-        tmem_ld_32x32b_x16(taddr + 32, v1);
-        tmem_wait_ld(v0);
-        tmem_wait_ld(v1);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            v[i] = v0[i];
+    for (int c = 0; c < NV / 16; ++c)
+        fma_cols<16>(acc + C0 + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(v + 16 * c),
+                     C0 + 16 * c < jb ? s0 : s1);
+}
+
+// The trade of halves (KSPLIT = 2): this CTA's partial of columns GIVE0 ..
+// GIVE0 + BN/2 goes to `out` ([BN/8 float4 columns][128 rows]); the
+// partner's partial of KEEP0 .. KEEP0 + BN/2 is read from `in` once `ready`
+// reaches 4 (its four epilogue warps) and added.  The warp that reads last
+// (`done` reaches 4) zeroes both counters for the next call.  Returns false
+// if the wait ran out.
+template <int GIVE0, int KEEP0, int BN>
+__device__ __forceinline__ bool trade_halves(float (&acc)[BN], float4 *out, const float4 *in, int *my_ready,
+                                             int *partner_ready, int *done, bool live, int row, int lane,
+                                             const WaitCtl &ctl)
+{
+    constexpr int C4 = BN / 8;
+    if (live) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            v[32 + i] = v1[i];
+        for (int c = 0; c < C4; ++c)
+            st_cg_f4(out + c * kBM + row, make_float4(acc[GIVE0 + 4 * c], acc[GIVE0 + 4 * c + 1],
+                                                     acc[GIVE0 + 4 * c + 2], acc[GIVE0 + 4 * c + 3]));
+    }
+    __threadfence();
+    __syncwarp();
+    int got = 1;
+    if (lane == 0) {
+        red_release_add(my_ready, 1);
+        got = wait_counter(partner_ready, 4, ctl) ? 1 : 0;
+    }
+    got = __shfl_sync(0xffffffffu, got, 0);
+    if (!got)
+        return false;
+    __syncwarp();
+    if (live) {
+#pragma unroll
+        for (int c = 0; c < C4; ++c) {
+            const float4 v = ld_cg_f4(in + c * kBM + row);
+            acc[KEEP0 + 4 * c] += v.x;
+            acc[KEEP0 + 4 * c + 1] += v.y;
+            acc[KEEP0 + 4 * c + 2] += v.z;
+            acc[KEEP0 + 4 * c + 3] += v.w;
+        }
+    }
+    __syncwarp();
+    if (lane == 0 && atomicAdd(done, 1) == 3) {
+        // every warp of this CTA has seen the partner's count: no one reads
+        // either counter again in this launch
+        *partner_ready = 0;
+        *done = 0;
+    }
+    return true;
+}
+
+// bf16 (round to nearest even) stores of NC columns of this thread's row,
+// acc[C0 ..] to D columns x0 .., 16 bytes at a time (N is a multiple of 16).
+template <int C0, int NC, int BN>
+__device__ __forceinline__ void store_row(const float (&acc)[BN], __nv_bfloat16 *drow, int x0, int N)
+{
+    uint4 *dst = reinterpret_cast<uint4 *>(drow + x0);
+#pragma unroll
+    for (int c = 0; c < NC / 8; ++c) {
+        if (x0 + 8 * c < N)
+            dst[c] = make_uint4(pack_bf16x2(acc[C0 + 8 * c], acc[C0 + 8 * c + 1]),
+                                pack_bf16x2(acc[C0 + 8 * c + 2], acc[C0 + 8 * c + 3]),
+                                pack_bf16x2(acc[C0 + 8 * c + 4], acc[C0 + 8 * c + 5]),
+                                pack_bf16x2(acc[C0 + 8 * c + 6], acc[C0 + 8 * c + 7]));
     }
 }
 
-template <int BN, int A_ROWS, int KD, int S>
-__global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S>::kThreads, 1)
+template <int BN, int A_ROWS, int KD, int S, int KSPLIT>
+__global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads, 1)
     fp8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                            const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                            const __grid_constant__ Params p)
 {
 #if defined(__CUDA_ARCH__)
-    using C = NarrowCfg<BN, A_ROWS, KD, S>;
+    using C = NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>;
     constexpr int BC = C::kBufCols;
     constexpr int NG = C::kGroups;
     constexpr int SR = C::kScaleSlots;
@@ -172,21 +243,27 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S>::kThreads, 1)
     grid_launch_dependents();
 
     const WaitCtl ctl{abort_flag, p.error_word, p.timeout_ns};
-    const int slices = p.num_n_blocks;
+    // work units: (slice, K part), unit u = KSPLIT * slice + part; a part is
+    // a whole number of scale chunks of K blocks (the last may be short or,
+    // for a very short K, empty)
+    const int units = p.num_n_blocks * KSPLIT;
+    const int kb_part = KSPLIT == 1 ? p.kb : ((p.kb + 1) / 2 + kScaleChunk - 1) / kScaleChunk * kScaleChunk;
+    auto kb_begin = [&](int u) { return (u % KSPLIT) * kb_part; };
+    auto kb_end = [&](int u) { return min(p.kb, (u % KSPLIT + 1) * kb_part); };
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
         Ring ring, sring;
         uint32_t issued = 0, issued_parity = 0, sissued = 0, sissued_parity = 0;
         bool ok = bounds_ok(p.a_box_rows == A_ROWS && p.rows <= A_ROWS, ctl);
-        for (int s = blockIdx.x; ok && s < slices; s += gridDim.x) {
-            const int b_row0 = s * BN;
+        for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            const int b_row0 = (u / KSPLIT) * BN;
             if (!bounds_ok(b_row0 < p.N, ctl)) {
                 ok = false;
                 break;
             }
             const int sfb0 = (b_row0 / 128) * p.kb;     // the slice's column block in the flat SFB
-            for (int k0 = 0; k0 < p.kb; k0 += KD) {
+            for (int k0 = kb_begin(u); k0 < kb_end(u); k0 += KD) {
                 if (!mbar_wait(&empty[ring.i], ring.ph ^ 1u, ctl)) {
                     ok = false;
                     break;
@@ -232,9 +309,10 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S>::kThreads, 1)
         Ring ring, acc;
         constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
         bool ok = true;
-        for (int s = blockIdx.x; ok && s < slices; s += gridDim.x) {
-            for (int k0 = 0; k0 < p.kb; k0 += KD) {
-                const int nk = min(KD, p.kb - k0);
+        for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            const int k_end = kb_end(u);
+            for (int k0 = kb_begin(u); k0 < k_end; k0 += KD) {
+                const int nk = min(KD, k_end - k0);
                 if (!mbar_wait(&tempty[acc.i], acc.ph ^ 1u, ctl) || !mbar_wait(&full[ring.i], ring.ph, ctl)) {
                     ok = false;
                     break;
@@ -273,8 +351,9 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S>::kThreads, 1)
         const bool quarter_live = p.rows > 32 * q;
         Ring ring, acc, sring;
         bool ok = true;
-        for (int s = blockIdx.x; ok && s < slices; s += gridDim.x) {
-            const int col0 = s * BN;
+        for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            const int col0 = (u / KSPLIT) * BN;
+            const int k_end = kb_end(u);
             const int sfb0 = (col0 / 128) * p.kb;
             // columns of the slice before the next 128-column block starts
             const int jb = 128 * (col0 / 128 + 1) - col0;
@@ -282,8 +361,8 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S>::kThreads, 1)
 #pragma unroll
             for (int i = 0; i < BN; ++i)
                 accum[i] = 0.f;
-            for (int k0 = 0; k0 < p.kb; k0 += KD) {
-                const int nk = min(KD, p.kb - k0);
+            for (int k0 = kb_begin(u); k0 < k_end; k0 += KD) {
+                const int nk = min(KD, k_end - k0);
                 const int kc0 = k0 % kScaleChunk;        // the group's place in its scale chunk
                 int got = 1;
                 if (lane == 0)
@@ -316,14 +395,25 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S>::kThreads, 1)
                             const float sa = pa[j * kBM];
                             const float s0 = sa * pb[j];
                             const float s1 = (C::kSfbRows > 1 && jb < BN) ? sa * pb1[j] : s0;
-                            uint32_t v[BN];
-                            narrow_ld<BN>(taddr + j * BC, v);
-                            if (j + 1 == nk)
-                                release_tmem(&tempty[acc.i], lane);
-#pragma unroll
-                            for (int c = 0; c < BN / 16; ++c)
-                                fma_cols<16>(accum + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(v + 16 * c),
-                                             16 * c < jb ? s0 : s1);
+                            // both pieces' loads in flight at once; the
+                            // buffers go back once both have landed
+                            uint32_t v0[C::kPiece0];
+                            tmem_ld(taddr + j * BC, v0);
+                            if constexpr (C::kPiece1 > 0) {
+                                uint32_t v1[C::kPiece1];
+                                tmem_ld(taddr + j * BC + C::kPiece0, v1);
+                                tmem_wait_ld(v0);
+                                tmem_wait_ld(v1);
+                                if (j + 1 == nk)
+                                    release_tmem(&tempty[acc.i], lane);
+                                promote_piece<0>(accum, v0, jb, s0, s1);
+                                promote_piece<C::kPiece0>(accum, v1, jb, s0, s1);
+                            } else {
+                                tmem_wait_ld(v0);
+                                if (j + 1 == nk)
+                                    release_tmem(&tempty[acc.i], lane);
+                                promote_piece<0>(accum, v0, jb, s0, s1);
+                            }
                         }
                     }
                 } else {
@@ -331,7 +421,7 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S>::kThreads, 1)
                 }
                 ring.template next<S>();
                 acc.template next<NG>();
-                if (kc0 + KD == kScaleChunk || k0 + KD >= p.kb) {
+                if (kc0 + KD == kScaleChunk || k0 + KD >= k_end) {
                     // the chunk's last group: its scale slot may be refilled
                     __syncwarp();
                     if (lane == 0)
@@ -341,16 +431,34 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S>::kThreads, 1)
             }
             if (!ok)
                 break;
-            // ---- bf16 row stores (16 bytes at a time; N is a multiple of 16)
-            if (row < p.rows && bounds_ok(row < p.d_rows_total, ctl)) {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.d + (size_t)row * p.N + col0);
-#pragma unroll
-                for (int c = 0; c < BN / 8; ++c) {
-                    if (col0 + 8 * c < p.N)
-                        dst[c] = make_uint4(pack_bf16x2(accum[8 * c], accum[8 * c + 1]),
-                                            pack_bf16x2(accum[8 * c + 2], accum[8 * c + 3]),
-                                            pack_bf16x2(accum[8 * c + 4], accum[8 * c + 5]),
-                                            pack_bf16x2(accum[8 * c + 6], accum[8 * c + 7]));
+            const bool live = row < p.rows && bounds_ok(row < p.d_rows_total, ctl);
+            __nv_bfloat16 *drow = p.d + (size_t)row * p.N;
+            if constexpr (KSPLIT == 1) {
+                if (live)
+                    store_row<0, BN>(accum, drow, col0, p.N);
+            } else {
+                // the trade of halves with the slice's other K part (unit u ^ 1)
+                constexpr int H = BN / 2;
+                if (!bounds_ok(u < units && (u ^ 1) < units, ctl)) {
+                    ok = false;
+                    break;
+                }
+                float4 *parts = reinterpret_cast<float4 *>(p.partials);
+                float4 *out = parts + (size_t)u * (BN / 8) * kBM;
+                const float4 *in = parts + (size_t)(u ^ 1) * (BN / 8) * kBM;
+                int *ready = p.counters, *done = p.counters + units;
+                const bool first = (u & 1) == 0;   // K part 0 keeps the slice's first half
+                ok = first ? trade_halves<H, 0>(accum, out, in, ready + u, ready + (u ^ 1), done + u, live, row,
+                                                lane, ctl)
+                           : trade_halves<0, H>(accum, out, in, ready + u, ready + (u ^ 1), done + u, live, row,
+                                                lane, ctl);
+                if (!ok)
+                    break;
+                if (live) {
+                    if (first)
+                        store_row<0, H>(accum, drow, col0, p.N);
+                    else
+                        store_row<H, H>(accum, drow, col0 + H, p.N);
                 }
             }
         }

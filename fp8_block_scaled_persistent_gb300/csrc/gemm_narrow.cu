@@ -1,7 +1,7 @@
 // gemm_narrow.cu -- launch of the narrow-slice kernel (gemm_kernel_narrow.cuh)
-// for the plain GEMM with M <= 128: one CTA per slice of narrow_block_n()
-// columns (the grid is min(slices, SMs); a CTA takes slices c, c + grid, ...),
-// 192 threads, programmatic stream serialisation.
+// for the plain GEMM with M <= 128: work units of one slice of
+// narrow_block_n() columns and one of narrow_ksplit() K parts (a CTA takes
+// units c, c + grid, ...), 192 threads, programmatic stream serialisation.
 #include <atomic>
 
 #include "gemm_kernel_narrow.cuh"
@@ -9,18 +9,26 @@
 #ifndef FP8G_PDL
 #define FP8G_PDL 1
 #endif
-// slice width and K blocks per copy, per A box height (64 rows: M <= 64)
+// slice width, K blocks per copy and K parts, per A box height (64 rows:
+// M <= 64).  With 128 rows every CTA reading all of A over the whole K range
+// makes A's copies rival B's, hence two K parts there.
 #ifndef FP8G_NARROW64_BN
 #define FP8G_NARROW64_BN 64
 #endif
 #ifndef FP8G_NARROW64_KD
 #define FP8G_NARROW64_KD 4
 #endif
+#ifndef FP8G_NARROW64_KSPLIT
+#define FP8G_NARROW64_KSPLIT 1
+#endif
 #ifndef FP8G_NARROW128_BN
-#define FP8G_NARROW128_BN 64
+#define FP8G_NARROW128_BN 96
 #endif
 #ifndef FP8G_NARROW128_KD
 #define FP8G_NARROW128_KD 2
+#endif
+#ifndef FP8G_NARROW128_KSPLIT
+#define FP8G_NARROW128_KSPLIT 2
 #endif
 #include "launch.h"
 
@@ -31,12 +39,12 @@ namespace {
 // as many stages as 192 KB of operands hold
 constexpr int stages_for(int bn, int a_rows, int kd) { return (192 * 1024) / (kd * (a_rows + bn) * kBK); }
 
-template <int BN, int A_ROWS, int KD>
+template <int BN, int A_ROWS, int KD, int KSPLIT>
 cudaError_t launch_narrow_one(const LaunchArgs &a)
 {
     constexpr int S = stages_for(BN, A_ROWS, KD);
-    using C = NarrowCfg<BN, A_ROWS, KD, S>;
-    auto kern = fp8_gemm_narrow_kernel<BN, A_ROWS, KD, S>;
+    using C = NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>;
+    auto kern = fp8_gemm_narrow_kernel<BN, A_ROWS, KD, S, KSPLIT>;
     static std::atomic<unsigned long long> attr_done{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -68,12 +76,14 @@ int narrow_block_n(int a_box_rows) { return a_box_rows == 64 ? FP8G_NARROW64_BN 
 
 int narrow_kd(int a_box_rows) { return a_box_rows == 64 ? FP8G_NARROW64_KD : FP8G_NARROW128_KD; }
 
+int narrow_ksplit(int a_box_rows) { return a_box_rows == 64 ? FP8G_NARROW64_KSPLIT : FP8G_NARROW128_KSPLIT; }
+
 cudaError_t launch_narrow(const LaunchArgs &a)
 {
     if (a.p.a_box_rows == 64)
-        return launch_narrow_one<FP8G_NARROW64_BN, 64, FP8G_NARROW64_KD>(a);
+        return launch_narrow_one<FP8G_NARROW64_BN, 64, FP8G_NARROW64_KD, FP8G_NARROW64_KSPLIT>(a);
     if (a.p.a_box_rows == 128)
-        return launch_narrow_one<FP8G_NARROW128_BN, 128, FP8G_NARROW128_KD>(a);
+        return launch_narrow_one<FP8G_NARROW128_BN, 128, FP8G_NARROW128_KD, FP8G_NARROW128_KSPLIT>(a);
     return cudaErrorInvalidValue;
 }
 

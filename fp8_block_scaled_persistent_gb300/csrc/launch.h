@@ -70,14 +70,18 @@ int ue8m0_pair_block_n();
 int ue8m0_pair_max_active(int dev);
 
 // The narrow-slice kernel for the plain GEMM with M <= 128 (gemm_narrow.cu):
-// one CTA per slice of narrow_block_n(a_box_rows) columns, the whole K range
-// each, no split.  a.p.a_box_rows (64 when M <= 64, else 128) picks the
-// instantiation; a.p.num_n_blocks counts slices; tmap_a and tmap_b view A and
-// B as [K/128][rows][128 B] with boxes of a_box_rows (A) or the slice width
-// (B) rows x narrow_kd(a_box_rows) K blocks; tmap_sfa and tmap_sfb are
-// make_maps'.
+// work units of one slice of narrow_block_n(a_box_rows) columns and one of
+// narrow_ksplit(a_box_rows) K parts.  a.p.a_box_rows (64 when M <= 64, else
+// 128) picks the instantiation; a.p.num_n_blocks counts slices; tmap_a and
+// tmap_b view A and B as [K/128][rows][128 B] with boxes of a_box_rows (A) or
+// the slice width (B) rows x narrow_kd(a_box_rows) K blocks; tmap_sfa and
+// tmap_sfb are make_maps'.  With two K parts: a.p.counters holds 2 x units
+// zeroed ints and a.p.partials units x 128 x block_n/2 fp32 (see
+// narrow_workspace_bytes), and a.grid is even and at most the SM count (the
+// two CTAs of a slice wait for each other).
 cudaError_t launch_narrow(const LaunchArgs &a);
 int narrow_block_n(int a_box_rows);
 int narrow_kd(int a_box_rows);
+int narrow_ksplit(int a_box_rows);
 
 }  // namespace fp8g

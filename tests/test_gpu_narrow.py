@@ -1,13 +1,15 @@
-"""The narrow-slice kernel (plain GEMM with M <= 128: one CTA per 64-column
-slice, the whole K range, no split) against the oracle, through the C ABI.
+"""The narrow-slice kernel (plain GEMM with M <= 128: one CTA per narrow
+column slice and K part) against the oracle, through the C ABI.
 
-fp8_gemm_set_narrow_mode(1) forces it wherever it applies (M <= 128, K >= 512);
-the cases cover both A box heights (M <= 64 and 65..128), ragged M, N not a
-multiple of 64 (a partly empty last slice), K block counts that leave a
-partial last copy, more slices than SMs (CTAs take slices in turn), exact
-integers (bit-identical), the allocation-free entry point, a CUDA graph, and
-the full-size small-M workloads under the automatic choice, on the split-K
-schedule as well.
+fp8_gemm_set_narrow_mode(1) forces it wherever it applies (M <= 128, K >= 512).
+With M <= 64 it runs 64-column slices over the whole K range; with 65..128
+rows, 96-column slices (which straddle the 128-column scale blocks) in two K
+parts whose CTAs trade halves of the slice through the workspace.  The cases
+cover both, ragged M, N not a multiple of the slice width, K block counts
+that leave a partial last copy or an empty second K part, more work units
+than SMs (CTAs take units in turn), exact integers (bit-identical), the
+allocation-free entry point, a CUDA graph, and the full-size small-M
+workloads under the automatic choice, on the split-K schedule as well.
 """
 import numpy as np
 import pytest
@@ -47,12 +49,14 @@ def test_narrow_shapes(M, N, K):
     check(got, _ref(p), f"narrow {M}x{N}x{K}")
 
 
-def test_narrow_more_slices_than_sms():
-    """200 slices: with one CTA per SM some CTAs take two slices in turn."""
-    p = wl.make_nt(8, 64 * 200, 512, seed=11)
+@pytest.mark.parametrize("M,N,K", [(8, 64 * 200, 512), (100, 96 * 100, 1024)])
+def test_narrow_more_units_than_sms(M, N, K):
+    """200 work units: with one CTA per SM some CTAs take two in turn (with
+    two K parts, both CTAs of a slice in the same round)."""
+    p = wl.make_nt(M, N, K, seed=11)
     got, st, dst = gu.run(p)
     assert st == 0 and dst == 0
-    check(got, _ref(p), "narrow 8x12800x512")
+    check(got, _ref(p), f"narrow {M}x{N}x{K}")
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 512), (64, 192, 1664), (7, 272, 3968)])
@@ -85,7 +89,11 @@ def test_narrow_noalloc_bit_identical():
     p = wl.make_nt(96, 1024, 4096, seed=12)
     t = gu.dev_tensors(p)
     D_ref = gu.new_d(p)
-    assert gu.call(p, t, D_ref) == 0
+    # with the workspace it asks for (the trade of halves needs one), so that
+    # both calls run the same schedule
+    ws = gu.workspace_for(p)
+    assert ws is not None
+    assert gu.call(p, t, D_ref, workspace=ws) == 0
     ref = gu.bits(D_ref)
     D = gu.new_d(p)
     assert fg.fp8_gemm_nt_noalloc(t["A"], t["SFA"], t["B"], t["SFB"], D, p.M, p.N, p.K) == 0
@@ -103,19 +111,21 @@ def test_narrow_graph_replay_bit_identical():
     import fp8_block_scaled_persistent_gb300 as fg
     probs = [wl.make_nt(64, 512, 2048, seed=6), wl.make_nt(128, 320, 1536, seed=7)]
     tens = [gu.dev_tensors(p) for p in probs]
+    wss = [gu.workspace_for(p) for p in probs]      # the second trades halves through it
+    assert wss[1] is not None
     side = torch.cuda.Stream()
     ref = [gu.new_d(p) for p in probs]
     with torch.cuda.stream(side):
-        for p, t, D in zip(probs, tens, ref):
-            assert gu.call(p, t, D, stream=side) == 0
+        for p, t, D, ws in zip(probs, tens, ref, wss):
+            assert gu.call(p, t, D, workspace=ws, stream=side) == 0
     side.synchronize()
     assert fg.fp8_gemm_get_device_error(side) == 0
     ref_bits = [gu.bits(D) for D in ref]
     outs = [gu.new_d(p) for p in probs]
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=side):
-        for p, t, D in zip(probs, tens, outs):
-            assert gu.call(p, t, D, stream=side) == 0
+        for p, t, D, ws in zip(probs, tens, outs, wss):
+            assert gu.call(p, t, D, workspace=ws, stream=side) == 0
     for _ in range(2):
         for D in outs:
             D.view(torch.int16).fill_(np.int16(np.uint16(gu.SENTINEL).view(np.int16)))
