@@ -244,26 +244,31 @@ int fp8_gemm_set_pair_mode(int mode);
 
 /*
  * Narrow-slice kernel choice for fp8_gemm_nt and fp8_gemm_nt_noalloc
- * (process-wide).  With M <= 128 the GEMM is one stream of B; the narrow-slice
- * kernel gives each CTA one 64-column slice of the output and the whole K
- * range (one CTA per slice, up to one per SM, slices taken in turn beyond
- * that), so no partial sums are published or reduced and the call needs no
- * workspace.  Each copy brings several consecutive K blocks of A and B;
- * the promotion with the scales is the same as everywhere else (DeepGEMM
- * fp8_gemm.cuh, fp8_gemm_kernel: per 128-wide K block, scale_a * scale_b).
+ * (process-wide).  With M <= 128 the GEMM is one stream of B.  The
+ * narrow-slice kernel gives each CTA one narrow column slice of the output
+ * and one K range (one CTA per SM, work units taken in turn beyond that):
+ *   M <= 64     64-column slices over the whole K range: no partial sums, no
+ *               workspace;
+ *   M 65..128   96-column slices in two K parts (each CTA reads half of A):
+ *               the two CTAs of a slice trade halves of their fp32 partials
+ *               through the workspace, each adds the other's (P0 + P1, the
+ *               same bits in either order) and stores its half.
+ * Each copy brings several consecutive K blocks of A and B; the promotion
+ * with the scales is the same as everywhere else (DeepGEMM fp8_gemm.cuh,
+ * fp8_gemm_kernel: per 128-wide K block, scale_a * scale_b).
  *   mode  1 : every fp8_gemm_nt / fp8_gemm_nt_noalloc call with M <= 128
- *             and K >= 512;
- *   mode  0 : the automatic choice (the default): M <= 64, at least 8 K
- *             blocks, and ceil(N/64) slices between half the SM count and
- *             the SM count;
+ *             and K >= 512 (and, for M > 64, a big enough workspace);
+ *   mode  0 : the automatic choice (the default): as mode 1, with at least
+ *             8 K blocks per K part and between half the SM count and the SM
+ *             count of work units;
  *   mode -1 : never.
  * A block_n or split override (fp8_gemm_set_override) rules it out.  Results
  * equal the other schedules' to within fp32 rounding order (bit-identical on
  * exactly representable inputs).  Returns FP8G_ERR_INVALID_ARG for other
  * values.  The environment variable FP8G_NARROW_MODE ("-1", "0" or "1"), read
  * when the library loads, sets the same value; this call replaces it.
- * fp8_gemm_workspace_size still reports the split-K schedule's workspace for
- * FP8G_KIND_NT (the addend variant, which never runs narrow, uses that size).
+ * fp8_gemm_workspace_size(FP8G_KIND_NT, ...) covers whichever of the split-K
+ * schedule and the two-part narrow schedule the call would run.
  */
 int fp8_gemm_set_narrow_mode(int mode);
 
