@@ -237,12 +237,7 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    // a programmatic dependent of the previous kernel on the stream: nothing
-    // in global memory is touched before that grid has completed
-    grid_dependency_wait();
-    grid_launch_dependents();
 
-    const WaitCtl ctl{abort_flag, p.error_word, p.timeout_ns};
     // work units: (slice, K part), unit u = KSPLIT * slice + part; a part is
     // a whole number of scale chunks of K blocks (the last may be short or,
     // for a very short K, empty)
@@ -250,6 +245,15 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
     const int kb_part = KSPLIT == 1 ? p.kb : ((p.kb + 1) / 2 + kScaleChunk - 1) / kScaleChunk * kScaleChunk;
     auto kb_begin = [&](int u) { return (u % KSPLIT) * kb_part; };
     auto kb_end = [&](int u) { return min(p.kb, (u % KSPLIT + 1) * kb_part); };
+    // a programmatic dependent of the previous kernel on the stream: nothing
+    // in global memory is read or written before that grid has completed.
+    // The next kernel is let in only once this CTA's last copy is issued
+    // (below): triggered at the start, its CTAs took the SMs this grid leaves
+    // idle for the whole launch (64 x 7168 x 16384: 27.1 -> 26.9 us, 128 x
+    // 7168 x 16384: 28.8 -> 28.4 us).
+    grid_dependency_wait();
+
+    const WaitCtl ctl{abort_flag, p.error_word, p.timeout_ns};
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
@@ -297,6 +301,7 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
                 }
             }
         }
+        grid_launch_dependents();
         // every copy this thread started has landed before the CTA exits
         for (int i = 0; i < S; ++i)
             if (issued & (1u << i))
