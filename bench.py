@@ -74,6 +74,16 @@ def bound_of(name):
     return "hbm" if name in HBM_BOUND else "tensor"
 
 
+def kernel_of(name):
+    """The library kernel the automatic choice runs for a workload (what the
+    launch lists in profiles/ show for it)."""
+    if name.startswith("smallm_"):
+        return "fp8_gemm_narrow_kernel"
+    if name.startswith("ue8m0_"):
+        return "fp8_gemm_ue8m0_pair_kernel"
+    return "fp8_gemm_kernel"
+
+
 def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
@@ -459,7 +469,7 @@ def run_ours(args, dist, ws, rank, local):
     dom = max(head, key=lambda e: e["ms"])
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     roof = {"bound": dom["bound"], "achieved": dom["achieved"], "peak": dom["peak"], "unit": dom["unit"],
-            "frac": dom["frac"], "traffic": dom["traffic"], "kernel": f"fp8_gemm_kernel ({dom['workload']})",
+            "frac": dom["frac"], "traffic": dom["traffic"], "kernel": f"{kernel_of(dom['workload'])} ({dom['workload']})",
             "ms_per_launch": dom["ms"],
             "peak_source": (f"{peaks['source']} HBM copy bandwidth" if dom["bound"] == "hbm" else
                             f"{peaks['source']} bf16 burst x {FP8_OVER_BF16} (nominal fp8/bf16)")}
