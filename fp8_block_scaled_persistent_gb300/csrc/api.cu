@@ -284,12 +284,9 @@ struct NtChoice {
 };
 
 // The narrow-slice kernel's launch shape for M rows: A box height, slice
-// width, K parts, units and the workspace its trade of halves needs (none
-// with one K part): 2 x units counters (256-byte aligned) then units x 128 x
-// block_n/2 fp32.
+// width, K parts and work units.
 struct NarrowShape {
     int a_rows, block_n, ksplit, slices, units;
-    size_t workspace;
 };
 
 NarrowShape narrow_shape(int M, int N)
@@ -300,31 +297,24 @@ NarrowShape narrow_shape(int M, int N)
     n.ksplit = fp8g::narrow_ksplit(n.a_rows);
     n.slices = ceil_div(N, n.block_n);
     n.units = n.slices * n.ksplit;
-    n.workspace = n.ksplit == 1 ? 0
-                                : ((size_t)2 * n.units * sizeof(int) + 255) / 256 * 256 +
-                                      (size_t)n.units * 128 * (n.block_n / 2) * sizeof(float);
     return n;
 }
 
 // Whether the narrow-slice kernel runs a plain GEMM (no addend) of M x N x K
-// on `sms` SMs with `workspace_bytes` of workspace (< 0: as much as it
-// needs): asked for (fp8_gemm_set_narrow_mode(1)) with M <= 128 and at least
-// 4 K blocks (its copies are up to 4 K blocks deep), or, automatically, with
-// at least 8 K blocks (16 with two K parts) when its units keep at least half
-// the SMs busy without needing a second round.  Measured on 64 / 128 x 7168 x
-// 16384 against the split-K schedule: one K part, 64-column slices for
+// on `sms` SMs: asked for (fp8_gemm_set_narrow_mode(1)) with M <= 128 and at
+// least 4 K blocks (its copies are up to 4 K blocks deep), or, automatically,
+// with at least 8 K blocks (16 with two K parts) when its units keep at least
+// half the SMs busy without needing a second round.  Measured on 64 / 128 x
+// 7168 x 16384 against the split-K schedule: one K part, 64-column slices for
 // M <= 64 (30.5 -> 27.1 us); with 65..128 rows every CTA reading all of A
 // over the whole K range was slower (32.6 against 32.2 us), hence two K
-// parts there.  A forced tile width or split rules it out, and so does a
-// workspace too small for the trade of halves.
-bool want_narrow(int M, int N, int K, int sms, long long workspace_bytes)
+// parts there.  A forced tile width or split rules it out.
+bool want_narrow(int M, int N, int K, int sms)
 {
     const int mode = g_narrow_mode.load();
     if (mode < 0 || M > 128 || K / 128 < 4 || g_override_bn.load() != 0 || g_override_split.load() > 0)
         return false;
     const NarrowShape n = narrow_shape(M, N);
-    if (workspace_bytes >= 0 && (long long)n.workspace > workspace_bytes)
-        return false;
     if (mode > 0)
         return true;
     const int cap = n.ksplit == 1 ? sms : (sms & ~1);
@@ -344,15 +334,14 @@ int choose_nt(int M, int N, int K, int sms, long long workspace_bytes, NtChoice 
     const int kb = K / 128;
     const int obn = g_override_bn.load();
     const int osplit = g_override_split.load();
-    if (allow_narrow && want_narrow(M, N, K, sms, workspace_bytes)) {
+    if (allow_narrow && want_narrow(M, N, K, sms)) {
         const NarrowShape n = narrow_shape(M, N);
         c.narrow = true;
         c.block_n = n.block_n;
         c.split_ctas = 0;
         c.tiles = n.units;
-        // with two K parts the two CTAs of a slice wait for each other: all
-        // resident, and an even grid keeps them in the same round
-        c.grid = n.ksplit == 1 ? std::min(sms, n.units) : std::min(sms & ~1, n.units);
+        // the launch sets the grid (two K parts: whole clusters that fit)
+        c.grid = std::min(sms, n.units);
         return FP8G_OK;
     }
     auto tiles_for = [&](int bn) { return mb * ceil_div(N, bn); };
@@ -549,10 +538,9 @@ int run_nt_pair(const void *A, const float *SFA, const void *B, const float *SFB
     return to_status(fp8g::launch_pair(C ? fp8g::kKindNTAcc : fp8g::kKindNT, bn, a));
 }
 
-// The plain GEMM (M <= 128, no addend) on the narrow-slice kernel; `scratch`
-// holds narrow_shape().workspace zeroed bytes when it trades halves.
+// The plain GEMM (M <= 128, no addend) on the narrow-slice kernel.
 int run_nt_narrow(const void *A, const float *SFA, const void *B, const float *SFB, void *D, int M, int N, int K,
-                  const NtChoice &c, void *scratch, const DeviceInfo &dev, fp8g_stream_t stream)
+                  const NtChoice &c, const DeviceInfo &dev, fp8g_stream_t stream)
 {
     const NarrowShape n = narrow_shape(M, N);
     LaunchArgs a;
@@ -560,12 +548,14 @@ int run_nt_narrow(const void *A, const float *SFA, const void *B, const float *S
     a.p.a_box_rows = n.a_rows;    // with M <= 64 rows past M are never stored: load only the first 64
     a.p.num_m_blocks = 1;
     a.p.num_tiles = c.tiles;
-    if (n.workspace) {
-        if (!scratch || !aligned(scratch, 256))
-            return scratch ? FP8G_ERR_MISALIGNED : FP8G_ERR_WORKSPACE;
-        const size_t counters = ((size_t)2 * n.units * sizeof(int) + 255) / 256 * 256;
-        a.p.counters = static_cast<int *>(scratch);
-        a.p.partials = reinterpret_cast<float *>(static_cast<char *>(scratch) + counters);
+    int grid = c.grid;
+    if (n.ksplit == 2) {
+        // clusters of two that are all resident at once; an even grid keeps
+        // both CTAs of a slice in the same round
+        const int clusters = fp8g::narrow_max_clusters(dev.id, n.a_rows);
+        if (clusters <= 0)
+            return FP8G_ERR_CUDA;
+        grid = std::min(n.units, 2 * clusters);
     }
     const uint32_t kd = (uint32_t)fp8g::narrow_kd(a.p.a_box_rows);
     std::memset(&a.tmap_d, 0, sizeof(a.tmap_d));
@@ -578,7 +568,7 @@ int run_nt_narrow(const void *A, const float *SFA, const void *B, const float *S
         !make_map(&a.tmap_sfb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SFB, (uint64_t)a.p.nb * a.p.kb, 0, 0,
                   fp8g::kScaleChunk + 4, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
         return FP8G_ERR_CUDA;
-    a.grid = c.grid;
+    a.grid = grid;
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     return to_status(fp8g::launch_narrow(a));
 }
@@ -596,7 +586,7 @@ int run_nt(const void *A, const float *SFA, const void *B, const float *SFB, con
     if ((st = choose_nt(M, N, K, dev.sms, ws, c, C == nullptr)) != FP8G_OK)
         return st;
     if (c.narrow)
-        return run_nt_narrow(A, SFA, B, SFB, D, M, N, K, c, workspace, dev, stream);
+        return run_nt_narrow(A, SFA, B, SFB, D, M, N, K, c, dev, stream);
     if (c.split_ctas && !aligned(workspace, 256))
         return FP8G_ERR_MISALIGNED;
     int pairs = 0;
@@ -856,15 +846,12 @@ size_t fp8_gemm_workspace_size(int kind, int M, int N, int K, int G)
     (void)G;
     if (kind != FP8G_KIND_NT || M <= 0 || N <= 0 || K <= 0 || K % 128 != 0)
         return 0;
-    // enough for whichever schedule fp8_gemm_nt or fp8_gemm_nt_accumulate
-    // picks: the split-K schedule's, or the narrow-slice kernel's trade of
-    // halves
+    // the split-K schedule's (fp8_gemm_nt_accumulate never runs the
+    // narrow-slice kernel, and that kernel needs none)
     NtChoice c;
-    size_t split = 0;
-    if (choose_nt(M, N, K, sms_or_default(), -1, c) == FP8G_OK && c.split_ctas)
-        split = split_workspace_bytes(M, N, K, c.block_n, c.split_ctas);
-    const size_t narrow = want_narrow(M, N, K, sms_or_default(), -1) ? narrow_shape(M, N).workspace : 0;
-    return std::max(split, narrow);
+    if (choose_nt(M, N, K, sms_or_default(), -1, c) != FP8G_OK || !c.split_ctas)
+        return 0;
+    return split_workspace_bytes(M, N, K, c.block_n, c.split_ctas);
 }
 
 size_t fp8_gemm_workspace_size_for(int M, int N, int K, int block_n, int split_ctas)
@@ -1018,17 +1005,8 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const float *SFA, const void *
     NtChoice c;
     if ((st = choose_nt(M, N, K, dev.sms, -1, c, true)) != FP8G_OK)
         return st;
-    if (c.narrow && narrow_shape(M, N).workspace > kNoAllocScratchBytes &&
-        (st = choose_nt(M, N, K, dev.sms, -1, c)) != FP8G_OK)
-        return st;      // the trade of halves would not fit: the other schedules
-    if (c.narrow) {
-        const NarrowShape n = narrow_shape(M, N);
-        // the array keeps the previous call's contents: the counters start at zero
-        if (n.workspace && cudaMemsetAsync(scratch, 0, (size_t)2 * n.units * sizeof(int),
-                                           reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-            return FP8G_ERR_CUDA;
-        return run_nt_narrow(A, SFA, B, SFB, D, M, N, K, c, scratch, dev, stream);
-    }
+    if (c.narrow)
+        return run_nt_narrow(A, SFA, B, SFB, D, M, N, K, c, dev, stream);
     if (c.split_ctas && split_workspace_bytes(M, N, K, c.block_n, c.split_ctas) > kNoAllocScratchBytes) {
         if (g_override_split.load() > 0)
             return FP8G_ERR_SCRATCH_LIMIT;

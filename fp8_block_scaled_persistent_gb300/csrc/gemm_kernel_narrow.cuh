@@ -15,14 +15,15 @@
 // slice, and every CTA's range lies inside one slice:
 //   KSPLIT = 1  each CTA streams B[BN slice rows][K] once and stores its
 //               outputs itself (nothing published);
-//   KSPLIT = 2  the two CTAs of a slice stream one K half each (half of A per
-//               CTA: with 128 rows of A, A's copies rival B's), then trade
-//               halves of the slice: each publishes the fp32 partial of the
-//               columns the other finalises, waits for the other's, adds it
-//               (P0 + P1: fp32 addition commutes, so both orders give the
-//               same bits) and stores its half.  All CTAs of the grid are
-//               resident (one per SM) and every CTA publishes before it
-//               waits, so the waits end.
+//   KSPLIT = 2  the two CTAs of a slice, a cluster of two, stream one K half
+//               each (half of A per CTA: with 128 rows of A, A's copies rival
+//               B's), then trade halves of the slice over distributed shared
+//               memory: each stores the fp32 partial of the columns the other
+//               finalises straight into the other's shared memory, waits for
+//               the other's, adds it (P0 + P1: fp32 addition commutes, so both
+//               orders give the same bits) and stores its half.  Every CTA
+//               sends before it waits, so the waits end; nothing goes through
+//               global memory, so no workspace.
 // A slice whose width does not divide 128 may straddle one boundary of the
 // 128-column scale blocks: its scale slots then hold both blocks' B scales
 // and each 16-column chunk of the slice takes its block's.  The narrow tile
@@ -82,8 +83,10 @@ struct NarrowCfg {
     static constexpr int kSlotSfaBytes = kScaleChunk * kBM * 4;
     static constexpr int kSlotBytes = kSlotSfaBytes + 128 * kSfbRows;
     static constexpr int kSlotTxBytes = kSlotSfaBytes + (kScaleChunk + 4) * 4 * kSfbRows;
-    static constexpr int kBarriers = 2 * S + kGroups + 2 * kScaleSlots + 1;
-    static constexpr int kSmemBytes = S * kStageBytes + kScaleSlots * kSlotBytes + kBarriers * 8 + 16 +
+    // KSPLIT = 2: the partner's traded half, [BN/8 float4 columns][128 rows]
+    static constexpr int kXBytes = KSPLIT == 2 ? (BN / 2) * kBM * 4 : 0;
+    static constexpr int kBarriers = 2 * S + kGroups + 2 * kScaleSlots + 1 + 2;
+    static constexpr int kSmemBytes = S * kStageBytes + kScaleSlots * kSlotBytes + kXBytes + kBarriers * 8 + 16 +
                                       1024 /* alignment slack */;
     static_assert(kABlockBytes % 1024 == 0 && kBBlockBytes % 1024 == 0 && kStageBytes % 1024 == 0 &&
                       kSlotBytes % 128 == 0,
@@ -113,51 +116,62 @@ __device__ __forceinline__ void promote_piece(float (&acc)[BN], const uint32_t (
                      C0 + 16 * c < jb ? s0 : s1);
 }
 
-// The trade of halves (KSPLIT = 2): this CTA's partial of columns GIVE0 ..
-// GIVE0 + BN/2 goes to `out` ([BN/8 float4 columns][128 rows]); the
-// partner's partial of KEEP0 .. KEEP0 + BN/2 is read from `in` once `ready`
-// reaches 4 (its four epilogue warps) and added.  The warp that reads last
-// (`done` reaches 4) zeroes both counters for the next call.  Returns false
-// if the wait ran out.
+// The trade of halves (KSPLIT = 2) over distributed shared memory.  This
+// warp's rows of columns GIVE0 .. GIVE0 + BN/2 go into the partner CTA's
+// buffer (`peer_xbuf`, a shared::cluster address; [BN/8 float4 columns][128
+// rows]) and its arrival on the partner's `peer_xfull` releases them; once
+// this CTA's `xfull` completes (the partner's four warps), the partner's
+// partial of KEEP0 .. KEEP0 + BN/2 is read from `xbuf` and added.  Before a
+// later round writes the partner's buffer again, `xempty` (the partner's
+// warps have read it) is awaited; after reading, this warp arrives on the
+// partner's `peer_xempty` only if another round follows, so no arrival can
+// reach a CTA that has exited.  Returns false if a wait ran out.
 template <int GIVE0, int KEEP0, int BN>
-__device__ __forceinline__ bool trade_halves(float (&acc)[BN], float4 *out, const float4 *in, int *my_ready,
-                                             int *partner_ready, int *done, bool live, int row, int lane,
-                                             const WaitCtl &ctl)
+__device__ __forceinline__ bool trade_halves(float (&acc)[BN], uint32_t peer_xbuf, const float4 *xbuf,
+                                             uint64_t *xfull, uint64_t *xempty, uint32_t peer_xfull,
+                                             uint32_t peer_xempty, uint32_t round, bool more, bool live, int row,
+                                             int lane, const WaitCtl &ctl)
 {
     constexpr int C4 = BN / 8;
-    if (live) {
-#pragma unroll
-        for (int c = 0; c < C4; ++c)
-            st_cg_f4(out + c * kBM + row, make_float4(acc[GIVE0 + 4 * c], acc[GIVE0 + 4 * c + 1],
-                                                     acc[GIVE0 + 4 * c + 2], acc[GIVE0 + 4 * c + 3]));
-    }
-    __threadfence();
-    __syncwarp();
     int got = 1;
-    if (lane == 0) {
-        red_release_add(my_ready, 1);
-        got = wait_counter(partner_ready, 4, ctl) ? 1 : 0;
-    }
+    if (round > 0 && lane == 0)
+        got = mbar_wait(xempty, (round - 1) & 1u, ctl) ? 1 : 0;
     got = __shfl_sync(0xffffffffu, got, 0);
     if (!got)
         return false;
     __syncwarp();
     if (live) {
 #pragma unroll
+        for (int c = 0; c < C4; ++c)
+            st_shared_cluster_f4(peer_xbuf + (uint32_t)(c * kBM + row) * 16u,
+                                 make_float4(acc[GIVE0 + 4 * c], acc[GIVE0 + 4 * c + 1], acc[GIVE0 + 4 * c + 2],
+                                             acc[GIVE0 + 4 * c + 3]));
+    }
+    fence_acq_rel_cluster();
+    __syncwarp();
+    if (lane == 0) {
+        mbar_arrive_release_cluster(peer_xfull);
+        got = mbar_wait(xfull, round & 1u, ctl) ? 1 : 0;
+    }
+    got = __shfl_sync(0xffffffffu, got, 0);
+    if (!got)
+        return false;
+    __syncwarp();
+    fence_acq_rel_cluster();
+    if (live) {
+#pragma unroll
         for (int c = 0; c < C4; ++c) {
-            const float4 v = ld_cg_f4(in + c * kBM + row);
+            const float4 v = xbuf[c * kBM + row];
             acc[KEEP0 + 4 * c] += v.x;
             acc[KEEP0 + 4 * c + 1] += v.y;
             acc[KEEP0 + 4 * c + 2] += v.z;
             acc[KEEP0 + 4 * c + 3] += v.w;
         }
     }
-    __syncwarp();
-    if (lane == 0 && atomicAdd(done, 1) == 3) {
-        // every warp of this CTA has seen the partner's count: no one reads
-        // either counter again in this launch
-        *partner_ready = 0;
-        *done = 0;
+    if (more) {
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive_release_cluster(peer_xempty);
     }
     return true;
 }
@@ -194,14 +208,17 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sm_stage = smem;                                   // S x [A | B]
     uint8_t *sm_scales = sm_stage + S * C::kStageBytes;         // SR scale slots
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm_scales + SR * C::kSlotBytes);
+    uint8_t *sm_xbuf = sm_scales + SR * C::kSlotBytes;          // KSPLIT = 2: the partner's traded half
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm_xbuf + C::kXBytes);
     uint64_t *full = bar;                  // S: a group's A/B tiles landed (TMA transactions)
     uint64_t *empty = full + S;            // S: the group's MMAs finished (stage free, partials ready)
     uint64_t *tempty = empty + S;          // NG: the epilogue read the group's buffers (4 warps)
     uint64_t *sfull = tempty + NG;         // SR: a scale chunk landed
     uint64_t *sempty = sfull + SR;         // SR: the epilogue is done with it (4 warps)
     uint64_t *drain = sempty + SR;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *xfull = drain + 1;           // KSPLIT = 2: the partner's half landed here (its 4 warps)
+    uint64_t *xempty = xfull + 1;          // KSPLIT = 2: the partner read this CTA's half (its 4 warps)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xempty + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -219,6 +236,8 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
             mbar_init(&sempty[i], 4);
         }
         mbar_init(drain, 1);
+        mbar_init(xfull, 4);
+        mbar_init(xempty, 4);
         *abort_flag = 0;
         fence_mbarrier_init();
         fence_proxy_async_shared();
@@ -235,6 +254,8 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
     }
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (KSPLIT == 2)
+        cluster_sync();     // the partner's barriers exist before anything reaches them
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -355,6 +376,8 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
         const int row = 32 * q + lane;           // row of A / D
         const bool quarter_live = p.rows > 32 * q;
         Ring ring, acc, sring;
+        uint32_t round = 0;     // units this CTA has traded so far
+        (void)round;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
             const int col0 = (u / KSPLIT) * BN;
@@ -442,21 +465,22 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
                 if (live)
                     store_row<0, BN>(accum, drow, col0, p.N);
             } else {
-                // the trade of halves with the slice's other K part (unit u ^ 1)
+                // the trade of halves with the slice's other K part (unit u ^ 1,
+                // the other CTA of this cluster: the grid is even, so both
+                // take their units in the same rounds)
                 constexpr int H = BN / 2;
-                if (!bounds_ok(u < units && (u ^ 1) < units, ctl)) {
-                    ok = false;
-                    break;
-                }
-                float4 *parts = reinterpret_cast<float4 *>(p.partials);
-                float4 *out = parts + (size_t)u * (BN / 8) * kBM;
-                const float4 *in = parts + (size_t)(u ^ 1) * (BN / 8) * kBM;
-                int *ready = p.counters, *done = p.counters + units;
+                const uint32_t peer = cluster_ctarank() ^ 1u;
+                const uint32_t peer_xbuf = mapa_shared(smem_u32(sm_xbuf), peer);
+                const uint32_t peer_xfull = mapa_shared(smem_u32(xfull), peer);
+                const uint32_t peer_xempty = mapa_shared(smem_u32(xempty), peer);
+                const float4 *xb = reinterpret_cast<const float4 *>(sm_xbuf);
+                const bool more = u + (int)gridDim.x < units;
                 const bool first = (u & 1) == 0;   // K part 0 keeps the slice's first half
-                ok = first ? trade_halves<H, 0>(accum, out, in, ready + u, ready + (u ^ 1), done + u, live, row,
-                                                lane, ctl)
-                           : trade_halves<0, H>(accum, out, in, ready + u, ready + (u ^ 1), done + u, live, row,
-                                                lane, ctl);
+                ok = first ? trade_halves<H, 0>(accum, peer_xbuf, xb, xfull, xempty, peer_xfull, peer_xempty,
+                                                round, more, live, row, lane, ctl)
+                           : trade_halves<0, H>(accum, peer_xbuf, xb, xfull, xempty, peer_xfull, peer_xempty,
+                                                round, more, live, row, lane, ctl);
+                ++round;
                 if (!ok)
                     break;
                 if (live) {
@@ -471,6 +495,11 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
 
     tc_fence_before_sync();
     __syncthreads();
+    // neither CTA of a trading pair leaves while the other may still store
+    // into its shared memory or arrive on its barriers (after a wait that ran
+    // out, too: every wait is bounded, so both get here)
+    if constexpr (KSPLIT == 2)
+        cluster_sync();
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, kTmemCols);

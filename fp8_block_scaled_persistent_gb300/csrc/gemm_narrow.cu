@@ -62,12 +62,56 @@ cudaError_t launch_narrow_one(const LaunchArgs &a)
     cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = a.stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = FP8G_PDL;
+    // two K parts: the two CTAs of a slice are a cluster (a.grid is even)
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = KSPLIT == 2 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, a.tmap_a, a.tmap_b, a.tmap_sfa, a.tmap_sfb, a.p);
+}
+
+// Clusters of two of an instantiation that can be resident at once on device
+// `dev` (cached; 0 on failure).
+template <int BN, int A_ROWS, int KD>
+int max_clusters_one(int dev)
+{
+    constexpr int S = stages_for(BN, A_ROWS, KD);
+    using C = NarrowCfg<BN, A_ROWS, KD, S, 2>;
+    static std::atomic<int> cache[64];
+    if (dev < 0 || dev >= 64)
+        return 0;
+    const int c = cache[dev].load();
+    if (c > 0)
+        return c;
+    auto kern = fp8_gemm_narrow_kernel<BN, A_ROWS, KD, S, 2>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+        return 0;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * sms, 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a.tmap_a, a.tmap_b, a.tmap_sfa, a.tmap_sfb, a.p);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 0;
+    }
+    cache[dev].store(n);
+    return n;
 }
 
 }  // namespace
@@ -77,6 +121,18 @@ int narrow_block_n(int a_box_rows) { return a_box_rows == 64 ? FP8G_NARROW64_BN 
 int narrow_kd(int a_box_rows) { return a_box_rows == 64 ? FP8G_NARROW64_KD : FP8G_NARROW128_KD; }
 
 int narrow_ksplit(int a_box_rows) { return a_box_rows == 64 ? FP8G_NARROW64_KSPLIT : FP8G_NARROW128_KSPLIT; }
+
+int narrow_max_clusters(int dev, int a_box_rows)
+{
+    if (a_box_rows == 64) {
+        if constexpr (FP8G_NARROW64_KSPLIT == 2)
+            return max_clusters_one<FP8G_NARROW64_BN, 64, FP8G_NARROW64_KD>(dev);
+        return 0;
+    }
+    if constexpr (FP8G_NARROW128_KSPLIT == 2)
+        return max_clusters_one<FP8G_NARROW128_BN, 128, FP8G_NARROW128_KD>(dev);
+    return 0;
+}
 
 cudaError_t launch_narrow(const LaunchArgs &a)
 {

@@ -75,13 +75,15 @@ int ue8m0_pair_max_active(int dev);
 // 128) picks the instantiation; a.p.num_n_blocks counts slices; tmap_a and
 // tmap_b view A and B as [K/128][rows][128 B] with boxes of a_box_rows (A) or
 // the slice width (B) rows x narrow_kd(a_box_rows) K blocks; tmap_sfa and
-// tmap_sfb are make_maps'.  With two K parts: a.p.counters holds 2 x units
-// zeroed ints and a.p.partials units x 128 x block_n/2 fp32 (see
-// narrow_workspace_bytes), and a.grid is even and at most the SM count (the
-// two CTAs of a slice wait for each other).
+// tmap_sfb are make_maps'.  With two K parts the two CTAs of a slice are a
+// cluster of two that trade halves over distributed shared memory: a.grid is
+// even and at most 2 x narrow_max_clusters().
 cudaError_t launch_narrow(const LaunchArgs &a);
 int narrow_block_n(int a_box_rows);
 int narrow_kd(int a_box_rows);
 int narrow_ksplit(int a_box_rows);
+// Clusters of two of the two-K-part instantiation for `a_box_rows` that can
+// be resident at once on device `dev` (0 on failure or with one K part).
+int narrow_max_clusters(int dev, int a_box_rows);
 
 }  // namespace fp8g

@@ -690,6 +690,27 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
+// Stores 16 bytes into the shared memory of a CTA of the cluster.
+__device__ __forceinline__ void st_shared_cluster_f4(uint32_t cluster_addr, float4 v)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+// Orders this thread's memory accesses at cluster scope (acquire and release).
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+// Arrives on an mbarrier of any CTA of the cluster with release semantics at
+// cluster scope: the arriving thread's earlier writes (including those
+// ordered before it by a cluster-scope fence) are visible to a thread that
+// observes the phase complete and then fences with acquire at cluster scope.
+__device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t bar_cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr)
+                 : "memory");
+}
+
 // Whole-cluster barrier (every thread of both CTAs), release/acquire.
 __device__ __forceinline__ void cluster_sync()
 {

@@ -247,17 +247,18 @@ int fp8_gemm_set_pair_mode(int mode);
  * (process-wide).  With M <= 128 the GEMM is one stream of B.  The
  * narrow-slice kernel gives each CTA one narrow column slice of the output
  * and one K range (one CTA per SM, work units taken in turn beyond that):
- *   M <= 64     64-column slices over the whole K range: no partial sums, no
- *               workspace;
+ *   M <= 64     64-column slices over the whole K range: no partial sums;
  *   M 65..128   96-column slices in two K parts (each CTA reads half of A):
- *               the two CTAs of a slice trade halves of their fp32 partials
- *               through the workspace, each adds the other's (P0 + P1, the
- *               same bits in either order) and stores its half.
+ *               the two CTAs of a slice, a cluster of two, trade halves of
+ *               their fp32 partials over distributed shared memory, each
+ *               adds the other's (P0 + P1, the same bits in either order)
+ *               and stores its half.
+ * It needs no workspace (a workspace passed in is left untouched).
  * Each copy brings several consecutive K blocks of A and B; the promotion
  * with the scales is the same as everywhere else (DeepGEMM fp8_gemm.cuh,
  * fp8_gemm_kernel: per 128-wide K block, scale_a * scale_b).
  *   mode  1 : every fp8_gemm_nt / fp8_gemm_nt_noalloc call with M <= 128
- *             and K >= 512 (and, for M > 64, a big enough workspace);
+ *             and K >= 512;
  *   mode  0 : the automatic choice (the default): as mode 1, with at least
  *             8 K blocks per K part and between half the SM count and the SM
  *             count of work units;
@@ -267,8 +268,9 @@ int fp8_gemm_set_pair_mode(int mode);
  * exactly representable inputs).  Returns FP8G_ERR_INVALID_ARG for other
  * values.  The environment variable FP8G_NARROW_MODE ("-1", "0" or "1"), read
  * when the library loads, sets the same value; this call replaces it.
- * fp8_gemm_workspace_size(FP8G_KIND_NT, ...) covers whichever of the split-K
- * schedule and the two-part narrow schedule the call would run.
+ * fp8_gemm_workspace_size(FP8G_KIND_NT, ...) still reports the split-K
+ * schedule's workspace (fp8_gemm_nt_accumulate, which never runs narrow,
+ * uses the same size).
  */
 int fp8_gemm_set_narrow_mode(int mode);
 

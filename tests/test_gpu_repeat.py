@@ -40,14 +40,8 @@ def test_repeated_launches_bit_identical(name, reps, narrow):
         assert np.array_equal(gu.bits(D), first), f"{name}: launch {i} differs from launch 0"
     if ws is not None:
         # the counters lead the workspace and are back at zero: 8 per
-        # 128-column tile on the split-K schedule; on the narrow-slice
-        # kernel's two K parts (65..128 rows), 2 per work unit (two per
-        # 96-column slice); with M <= 64 it uses none
-        if narrow == 1 and p.M > 64:
-            n_ctr = 2 * 2 * ((p.N + 95) // 96)
-        elif narrow == 1:
-            n_ctr = 0
-        else:
-            n_ctr = ((p.M + 127) // 128) * ((p.N + 127) // 128) * 8
+        # 128-column tile on the split-K schedule (the narrow-slice kernel
+        # uses none)
+        n_ctr = 0 if narrow == 1 else ((p.M + 127) // 128) * ((p.N + 127) // 128) * 8
         assert int(ws[: n_ctr * 4].view(torch.int32).abs().sum()) == 0
     fg.fp8_gemm_set_narrow_mode(0)
