@@ -207,9 +207,9 @@ def fp8_gemm_set_pair_mode(mode=0) -> int:
 
 def fp8_gemm_set_narrow_mode(mode=0) -> int:
     """1: every plain GEMM with M <= 128 runs on the narrow-slice kernel (one
-    CTA per narrow column slice: whole K for M <= 64, two K parts in
-    clusters of two trading halves over distributed shared memory above),
-    0: automatic choice, -1: never.
+    CTA per 96-column slice and K half, the two CTAs of a slice a cluster
+    trading halves over distributed shared memory), 0: automatic choice,
+    -1: never.
     Returns the status code."""
     return library().fp8_gemm_set_narrow_mode(int(mode))
 

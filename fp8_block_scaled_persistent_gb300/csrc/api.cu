@@ -305,10 +305,9 @@ NarrowShape narrow_shape(int M, int N)
 // least 4 K blocks (its copies are up to 4 K blocks deep), or, automatically,
 // with at least 8 K blocks (16 with two K parts) when its units keep at least
 // half the SMs busy without needing a second round.  Measured on 64 / 128 x
-// 7168 x 16384 against the split-K schedule: one K part, 64-column slices for
-// M <= 64 (30.5 -> 27.1 us); with 65..128 rows every CTA reading all of A
-// over the whole K range was slower (32.6 against 32.2 us), hence two K
-// parts there.  A forced tile width or split rules it out.
+// 7168 x 16384 against the split-K schedule (30.5 / 32.2 us): 96-column
+// slices in two K parts, 25.6 / 27.6 us.  A forced tile width or split rules
+// it out.
 bool want_narrow(int M, int N, int K, int sms)
 {
     const int mode = g_narrow_mode.load();

@@ -606,7 +606,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // before the previous grid has completed and its writes are visible.  The
     // next kernel may then be scheduled as SMs free up.
     grid_dependency_wait();
-    grid_launch_dependents();
 
     const WaitCtl ctl{abort_flag, p.error_word, p.timeout_ns,
                       SHARE ? mapa_shared(smem_u32(const_cast<int *>(abort_flag)), rank ^ 1u) : 0u};
@@ -699,6 +698,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     ring.template next<S>();
                 }
             }
+            // the next kernel on the stream is let in once this CTA's last
+            // copy is issued (at the start, its CTAs took the SMs this grid
+            // leaves idle; masked 16 x 256 x 7168 x 2048: 56.8 -> 55.8 us)
+            grid_launch_dependents();
             // every fill this thread started has landed before the CTA exits
             for (int i = 0; i < S; ++i)
                 if (issued & (1u << i))

@@ -10,16 +10,18 @@
 #define FP8G_PDL 1
 #endif
 // slice width, K blocks per copy and K parts, per A box height (64 rows:
-// M <= 64).  With 128 rows every CTA reading all of A over the whole K range
-// makes A's copies rival B's, hence two K parts there.
+// M <= 64).  Two K parts halve each CTA's share of A (with 128 rows A's
+// copies otherwise rival B's) and let 150 CTAs rather than 112 stream B;
+// measured on 64 x 7168 x 16384, 64-column slices over the whole K range
+// took 26.9 us, 96-column slices in two K parts 25.6 us.
 #ifndef FP8G_NARROW64_BN
-#define FP8G_NARROW64_BN 64
+#define FP8G_NARROW64_BN 96
 #endif
 #ifndef FP8G_NARROW64_KD
-#define FP8G_NARROW64_KD 4
+#define FP8G_NARROW64_KD 2
 #endif
 #ifndef FP8G_NARROW64_KSPLIT
-#define FP8G_NARROW64_KSPLIT 1
+#define FP8G_NARROW64_KSPLIT 2
 #endif
 #ifndef FP8G_NARROW128_BN
 #define FP8G_NARROW128_BN 96

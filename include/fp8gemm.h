@@ -245,15 +245,12 @@ int fp8_gemm_set_pair_mode(int mode);
 /*
  * Narrow-slice kernel choice for fp8_gemm_nt and fp8_gemm_nt_noalloc
  * (process-wide).  With M <= 128 the GEMM is one stream of B.  The
- * narrow-slice kernel gives each CTA one narrow column slice of the output
- * and one K range (one CTA per SM, work units taken in turn beyond that):
- *   M <= 64     64-column slices over the whole K range: no partial sums;
- *   M 65..128   96-column slices in two K parts (each CTA reads half of A):
- *               the two CTAs of a slice, a cluster of two, trade halves of
- *               their fp32 partials over distributed shared memory, each
- *               adds the other's (P0 + P1, the same bits in either order)
- *               and stores its half.
- * It needs no workspace (a workspace passed in is left untouched).
+ * narrow-slice kernel gives each CTA one 96-column slice of the output and
+ * one of two K parts (each CTA reads half of A; one CTA per SM, work units
+ * taken in turn beyond that).  The two CTAs of a slice, a cluster of two,
+ * trade halves of their fp32 partials over distributed shared memory; each
+ * adds the other's (P0 + P1, the same bits in either order) and stores its
+ * half.  It needs no workspace (a workspace passed in is left untouched).
  * Each copy brings several consecutive K blocks of A and B; the promotion
  * with the scales is the same as everywhere else (DeepGEMM fp8_gemm.cuh,
  * fp8_gemm_kernel: per 128-wide K block, scale_a * scale_b).

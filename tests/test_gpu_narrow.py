@@ -2,10 +2,10 @@
 column slice and K part) against the oracle, through the C ABI.
 
 fp8_gemm_set_narrow_mode(1) forces it wherever it applies (M <= 128, K >= 512).
-With M <= 64 it runs 64-column slices over the whole K range; with 65..128
-rows, 96-column slices (which straddle the 128-column scale blocks) in two K
-parts: the two CTAs of a slice are a cluster and trade halves of their fp32
-partials over distributed shared memory (no workspace).  The cases
+It runs 96-column slices (which straddle the 128-column scale blocks) in two
+K parts: the two CTAs of a slice are a cluster and trade halves of their fp32
+partials over distributed shared memory (no workspace); A boxes of 64 rows
+for M <= 64, 128 above.  The cases
 cover both, ragged M, N not a multiple of the slice width, K block counts
 that leave a partial last copy or an empty second K part, more work units
 than SMs (CTAs take units in turn), exact integers (bit-identical), the
