@@ -563,9 +563,9 @@ int run_nt_narrow(const void *A, const float *SFA, const void *B, const float *S
     if (!make_kblock_map(&a.tmap_a, A, (uint64_t)M, K, (uint32_t)a.p.a_box_rows, kd) ||
         !make_kblock_map(&a.tmap_b, B, (uint64_t)N, K, (uint32_t)c.block_n, kd) ||
         !make_map(&a.tmap_sfa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SFA, a.p.sfa_ld, a.p.kb, (uint64_t)a.p.sfa_ld * 4,
-                  128, fp8g::kScaleChunk, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                  128, (uint32_t)fp8g::narrow_scale_chunk(), CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(&a.tmap_sfb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SFB, (uint64_t)a.p.nb * a.p.kb, 0, 0,
-                  fp8g::kScaleChunk + 4, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+                  (uint32_t)fp8g::narrow_scale_chunk() + 4, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
         return FP8G_ERR_CUDA;
     a.grid = grid;
     a.stream = reinterpret_cast<cudaStream_t>(stream);

@@ -35,7 +35,7 @@
 // 192 threads (six warps):
 //   warp 0      TMA producer: per group one box of A (KD x A_ROWS rows x
 //               128 B) and one of B (KD x BN rows x 128 B), 128-byte swizzled,
-//               into an S-stage ring; the scales of kScaleChunk K blocks at a
+//               into an S-stage ring; the scales of kNarrowChunk K blocks at a
 //               time (128 A scales per K block, the slice's B scales) into a
 //               scale ring.
 //   warp 1      MMA issuer (and tensor-memory owner): per group, 4 x
@@ -59,14 +59,21 @@
 
 #include "gemm_kernel.cuh"
 
+// K blocks per scale copy (a multiple of the K blocks per operand copy)
+#ifndef FP8G_NARROW_CHUNK
+#define FP8G_NARROW_CHUNK 8
+#endif
+
 namespace fp8g {
+
+constexpr int kNarrowChunk = FP8G_NARROW_CHUNK;
 
 template <int BN, int A_ROWS, int KD, int S, int KSPLIT>
 struct NarrowCfg {
     static_assert(BN == 48 || BN == 64 || BN == 96, "slice width");
     static_assert(KSPLIT == 1 || (KSPLIT == 2 && BN % 32 == 0), "K parts (a traded half is whole float4s)");
     static_assert(A_ROWS == 64 || A_ROWS == 128, "A box rows");
-    static_assert(KD == 2 || KD == 4, "K blocks per copy (a divisor of kScaleChunk)");
+    static_assert((KD == 2 || KD == 4) && kNarrowChunk % KD == 0, "K blocks per copy (a divisor of the chunk)");
     static constexpr int kBN = BN;                          // output columns (B rows) per CTA
     static constexpr int kBufCols = BN <= 64 ? 64 : 128;    // tensor-memory columns per K block
     // 128-column scale blocks a slice can touch
@@ -79,10 +86,11 @@ struct NarrowCfg {
     static constexpr int kBBytes = KD * kBBlockBytes;
     static constexpr int kStageBytes = kABytes + kBBytes;   // A then B
     static constexpr int kGroups = kTmemCols / (KD * kBufCols);    // tensor-memory groups
-    static constexpr int kScaleSlots = 4;
-    static constexpr int kSlotSfaBytes = kScaleChunk * kBM * 4;
+    static constexpr int kScaleSlots = 32 / kNarrowChunk;      // 32 K blocks of scales in flight
+    static constexpr int kSlotSfaBytes = kNarrowChunk * kBM * 4;
     static constexpr int kSlotBytes = kSlotSfaBytes + 128 * kSfbRows;
-    static constexpr int kSlotTxBytes = kSlotSfaBytes + (kScaleChunk + 4) * 4 * kSfbRows;
+    static constexpr int kSlotTxBytes = kSlotSfaBytes + (kNarrowChunk + 4) * 4 * kSfbRows;
+    static_assert((kNarrowChunk + 4) * 4 <= 128, "a B scale row of a slot");
     // KSPLIT = 2: the partner's traded half, [BN/8 float4 columns][128 rows]
     static constexpr int kXBytes = KSPLIT == 2 ? (BN / 2) * kBM * 4 : 0;
     static constexpr int kBarriers = 2 * S + kGroups + 2 * kScaleSlots + 1 + 2;
@@ -263,7 +271,7 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
     // a whole number of scale chunks of K blocks (the last may be short or,
     // for a very short K, empty)
     const int units = p.num_n_blocks * KSPLIT;
-    const int kb_part = KSPLIT == 1 ? p.kb : ((p.kb + 1) / 2 + kScaleChunk - 1) / kScaleChunk * kScaleChunk;
+    const int kb_part = KSPLIT == 1 ? p.kb : ((p.kb + 1) / 2 + kNarrowChunk - 1) / kNarrowChunk * kNarrowChunk;
     auto kb_begin = [&](int u) { return (u % KSPLIT) * kb_part; };
     auto kb_end = [&](int u) { return min(p.kb, (u % KSPLIT + 1) * kb_part); };
     // a programmatic dependent of the previous kernel on the stream: nothing
@@ -302,7 +310,7 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
                 issued |= 1u << ring.i;
                 issued_parity = (issued_parity & ~(1u << ring.i)) | (ring.ph << ring.i);
                 ring.template next<S>();
-                if (k0 % kScaleChunk == 0) {
+                if (k0 % kNarrowChunk == 0) {
                     if (!mbar_wait(&sempty[sring.i], sring.ph ^ 1u, ctl)) {
                         ok = false;
                         break;
@@ -391,7 +399,7 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
                 accum[i] = 0.f;
             for (int k0 = kb_begin(u); k0 < k_end; k0 += KD) {
                 const int nk = min(KD, k_end - k0);
-                const int kc0 = k0 % kScaleChunk;        // the group's place in its scale chunk
+                const int kc0 = k0 % kNarrowChunk;       // the group's place in its scale chunk
                 int got = 1;
                 if (lane == 0)
                     got = ((kc0 != 0 || mbar_wait(&sfull[sring.i], sring.ph, ctl)) &&
@@ -449,7 +457,7 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
                 }
                 ring.template next<S>();
                 acc.template next<NG>();
-                if (kc0 + KD == kScaleChunk || k0 + KD >= k_end) {
+                if (kc0 + KD == kNarrowChunk || k0 + KD >= k_end) {
                     // the chunk's last group: its scale slot may be refilled
                     __syncwarp();
                     if (lane == 0)

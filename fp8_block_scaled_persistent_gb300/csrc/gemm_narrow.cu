@@ -122,6 +122,8 @@ int narrow_block_n(int a_box_rows) { return a_box_rows == 64 ? FP8G_NARROW64_BN 
 
 int narrow_kd(int a_box_rows) { return a_box_rows == 64 ? FP8G_NARROW64_KD : FP8G_NARROW128_KD; }
 
+int narrow_scale_chunk() { return kNarrowChunk; }
+
 int narrow_ksplit(int a_box_rows) { return a_box_rows == 64 ? FP8G_NARROW64_KSPLIT : FP8G_NARROW128_KSPLIT; }
 
 int narrow_max_clusters(int dev, int a_box_rows)

@@ -82,6 +82,8 @@ cudaError_t launch_narrow(const LaunchArgs &a);
 int narrow_block_n(int a_box_rows);
 int narrow_kd(int a_box_rows);
 int narrow_ksplit(int a_box_rows);
+// K blocks per scale copy: tmap_sfa boxes of 128 x this, tmap_sfb of this + 4.
+int narrow_scale_chunk();
 // Clusters of two of the two-K-part instantiation for `a_box_rows` that can
 // be resident at once on device `dev` (0 on failure or with one K part).
 int narrow_max_clusters(int dev, int a_box_rows);
