@@ -39,6 +39,9 @@ int main(void)
     CHECK(fp8_gemm_nt_noalloc(p, buf, p, buf, buf, 128, 256, 500, NULL) == FP8G_ERR_UNSUPPORTED);
     CHECK(fp8_gemm_set_override(100, 0) == FP8G_ERR_INVALID_ARG);
     CHECK(fp8_gemm_set_override(0, 0) == FP8G_OK);
+    CHECK(fp8_gemm_set_narrow_mode(2) == FP8G_ERR_INVALID_ARG);
+    CHECK(fp8_gemm_set_narrow_mode(-1) == FP8G_OK);
+    CHECK(fp8_gemm_set_narrow_mode(0) == FP8G_OK);
     CHECK(fp8_gemm_set_wait_timeout_ns(10) == FP8G_ERR_INVALID_ARG);
     CHECK(fp8_gemm_workspace_size_for(128, 256, 1024, 128, 10) == 256 + 2 * 10 * 128 * 128 * 4);
     printf("ok\n");
