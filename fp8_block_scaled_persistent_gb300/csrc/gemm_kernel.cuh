@@ -875,11 +875,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // with the addend/store warp: wait for half rd of C, add it and,
             // for the first half, hand the staging area back
             auto take_c = [&](int rd) -> bool {
-                int got = 1;
-                if (lane == 0)
-                    got = mbar_wait(c_full, cph, ctl) ? 1 : 0;
-                got = __shfl_sync(0xffffffffu, got, 0);
-                if (!got)
+                if (!warp_wait(c_full, cph, ctl))
                     return false;
                 cph ^= 1u;
                 __syncwarp();
@@ -910,18 +906,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 // buffer this warp frees after block k+S-NACC >= k.
                 const int kc = (k - w.kb0) % kScaleChunk;     // position in the scale chunk
                 const int k0 = k - kc;
-                int got = 1;
-                if (lane == 0)
-                    got = ((kc != 0 || mbar_wait(&sfull[sring.i], sring.ph, ctl)) &&
-                           mbar_wait(&empty[ring.i], ring.ph, ctl))
-                              ? 1
-                              : 0;
-                got = __shfl_sync(0xffffffffu, got, 0);
-                if (!got) {
+                if (!warp_all((kc != 0 || mbar_wait(&sfull[sring.i], sring.ph, ctl)) &&
+                              mbar_wait(&empty[ring.i], ring.ph, ctl))) {
                     ok = false;
                     break;
                 }
-                __syncwarp();           // orders lane 0's barrier waits before every lane's reads
+                __syncwarp();
                 tc_fence_after_sync();
                 // the scales are read inside promote_block, after the first
                 // TMEM load is issued; the B part starts at the aligned group

@@ -141,11 +141,7 @@ __device__ __forceinline__ bool trade_halves(float (&acc)[BN], uint32_t peer_xbu
                                              int lane, const WaitCtl &ctl)
 {
     constexpr int C4 = BN / 8;
-    int got = 1;
-    if (round > 0 && lane == 0)
-        got = mbar_wait(xempty, (round - 1) & 1u, ctl) ? 1 : 0;
-    got = __shfl_sync(0xffffffffu, got, 0);
-    if (!got)
+    if (round > 0 && !warp_wait(xempty, (round - 1) & 1u, ctl))
         return false;
     __syncwarp();
     if (live) {
@@ -157,12 +153,9 @@ __device__ __forceinline__ bool trade_halves(float (&acc)[BN], uint32_t peer_xbu
     }
     fence_acq_rel_cluster();
     __syncwarp();
-    if (lane == 0) {
+    if (lane == 0)
         mbar_arrive_release_cluster(peer_xfull);
-        got = mbar_wait(xfull, round & 1u, ctl) ? 1 : 0;
-    }
-    got = __shfl_sync(0xffffffffu, got, 0);
-    if (!got)
+    if (!warp_wait(xfull, round & 1u, ctl))
         return false;
     __syncwarp();
     fence_acq_rel_cluster();
@@ -400,14 +393,8 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
             for (int k0 = kb_begin(u); k0 < k_end; k0 += KD) {
                 const int nk = min(KD, k_end - k0);
                 const int kc0 = k0 % kNarrowChunk;       // the group's place in its scale chunk
-                int got = 1;
-                if (lane == 0)
-                    got = ((kc0 != 0 || mbar_wait(&sfull[sring.i], sring.ph, ctl)) &&
-                           mbar_wait(&empty[ring.i], ring.ph, ctl))
-                              ? 1
-                              : 0;
-                got = __shfl_sync(0xffffffffu, got, 0);
-                if (!got) {
+                if (!warp_all((kc0 != 0 || mbar_wait(&sfull[sring.i], sring.ph, ctl)) &&
+                              mbar_wait(&empty[ring.i], ring.ph, ctl))) {
                     ok = false;
                     break;
                 }

@@ -452,14 +452,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
             for (int k = 0; k < p.kb; ++k) {
                 const int kc = k % kScaleChunk;
-                int got = 1;
-                if (lane == 0)
-                    got = ((kc != 0 || mbar_wait(&sfull[sring.i], sring.ph, ctl)) &&
-                           mbar_wait(&empty[ring.i], ring.ph, ctl))
-                              ? 1
-                              : 0;
-                got = __shfl_sync(0xffffffffu, got, 0);
-                if (!got) {
+                if (!warp_all((kc != 0 || mbar_wait(&sfull[sring.i], sring.ph, ctl)) &&
+                              mbar_wait(&empty[ring.i], ring.ph, ctl))) {
                     ok = false;
                     break;
                 }

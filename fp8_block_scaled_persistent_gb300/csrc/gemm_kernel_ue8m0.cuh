@@ -224,11 +224,7 @@ __global__ void __launch_bounds__(Ue8m0Cfg::kThreads, 1)
         Work w;
         uint32_t acc_ph = 0;
         while (sched.next(w)) {
-            int got = 1;
-            if (lane == 0)
-                got = mbar_wait(acc_full, acc_ph, ctl) ? 1 : 0;
-            got = __shfl_sync(0xffffffffu, got, 0);
-            if (!got)
+            if (!warp_wait(acc_full, acc_ph, ctl))
                 break;
             __syncwarp();
             tc_fence_after_sync();
@@ -299,11 +295,7 @@ __global__ void __launch_bounds__(Ue8m0Cfg::kThreads, 1)
             }
             for (int k0 = 0; k0 < p.kb; k0 += C::kChunk) {
                 const int n = min(C::kChunk, p.kb - k0);
-                int got = 1;
-                if (lane == 0)
-                    got = mbar_wait(&sc_empty[sring.i], sring.ph ^ 1u, ctl) ? 1 : 0;
-                got = __shfl_sync(0xffffffffu, got, 0);
-                if (!got) {
+                if (!warp_wait(&sc_empty[sring.i], sring.ph ^ 1u, ctl)) {
                     ok = false;
                     break;
                 }
