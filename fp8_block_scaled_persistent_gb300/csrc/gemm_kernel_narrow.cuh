@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm_xbuf + C::kXBytes);
     uint64_t *full = bar;                  // S: a group's A/B tiles landed (TMA transactions)
     uint64_t *empty = full + S;            // S: the group's MMAs finished (stage free, partials ready)
-    uint64_t *tempty = empty + S;          // NG: the epilogue read the group's buffers (4 warps)
+    uint64_t *tempty = empty + S;          // NG: the epilogue read the group's buffers (4 warps x 32 lanes)
     uint64_t *sfull = tempty + NG;         // SR: a scale chunk landed
     uint64_t *sempty = sfull + SR;         // SR: the epilogue is done with it (4 warps)
     uint64_t *drain = sempty + SR;
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < NG; ++i)
-            mbar_init(&tempty[i], 4);
+            mbar_init(&tempty[i], 4 * 32);      // every lane of the 4 epilogue warps
         for (int i = 0; i < SR; ++i) {
             mbar_init(&sfull[i], 1);
             mbar_init(&sempty[i], 4);
