@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_init(&tempty[i], kNumEpiWarps * 32);   // every lane of every epilogue warp
         for (int i = 0; i < SR; ++i) {
             mbar_init(&sfull[i], 1);
-            mbar_init(&sempty[i], kNumEpiWarps);
+            mbar_init(&sempty[i], kNumEpiWarps * 32);   // every lane of every epilogue warp
         }
         mbar_init(drain, 1);
         mbar_init(c_full, 1);
@@ -934,10 +934,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 ring.template next<S>();
                 if (kc == kScaleChunk - 1 || k + 1 == w.kb1) {
                     // last K block of the chunk: the slot may be refilled
-                    // (released after the TMEM buffer, off its critical path)
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&sempty[sring.i]);
+                    // (released after the TMEM buffer, off its critical path;
+                    // every lane arrives)
+                    mbar_arrive(&sempty[sring.i]);
                     sring.template next<SR>();
                 }
                 if constexpr (kHelperC) {

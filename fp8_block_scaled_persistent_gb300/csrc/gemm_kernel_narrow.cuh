@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
     uint64_t *empty = full + S;            // S: the group's MMAs finished (stage free, partials ready)
     uint64_t *tempty = empty + S;          // NG: the epilogue read the group's buffers (4 warps x 32 lanes)
     uint64_t *sfull = tempty + NG;         // SR: a scale chunk landed
-    uint64_t *sempty = sfull + SR;         // SR: the epilogue is done with it (4 warps)
+    uint64_t *sempty = sfull + SR;         // SR: the epilogue is done with it (4 warps x 32 lanes)
     uint64_t *drain = sempty + SR;
     uint64_t *xfull = drain + 1;           // KSPLIT = 2: the partner's half landed here (its 4 warps)
     uint64_t *xempty = xfull + 1;          // KSPLIT = 2: the partner read this CTA's half (its 4 warps)
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
             mbar_init(&tempty[i], 4 * 32);      // every lane of the 4 epilogue warps
         for (int i = 0; i < SR; ++i) {
             mbar_init(&sfull[i], 1);
-            mbar_init(&sempty[i], 4);
+            mbar_init(&sempty[i], 4 * 32);      // every lane of the 4 epilogue warps
         }
         mbar_init(drain, 1);
         mbar_init(xfull, 4);
@@ -446,9 +446,8 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
                 acc.template next<NG>();
                 if (kc0 + KD == kNarrowChunk || k0 + KD >= k_end) {
                     // the chunk's last group: its scale slot may be refilled
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&sempty[sring.i]);
+                    // (every lane arrives)
+                    mbar_arrive(&sempty[sring.i]);
                     sring.template next<SR>();
                 }
             }
