@@ -33,7 +33,9 @@
 //               acc += (sa*sb) * P in fp32 registers (one row per thread,
 //               BN/2 columns per warp), and at the end of a tile bf16
 //               conversion into swizzled staging panels and TMA stores (or
-//               predicated stores where masked rows straddle).
+//               predicated stores where masked rows straddle).  Every lane
+//               waits on the MMA completion itself and every lane arrives on
+//               the buffer's release (see warp_wait in ptx.cuh).
 // Registers: the control warpgroup drops to kRegsCtl with setmaxnreg and the
 // epilogue warpgroups rise to kRegsEpi (the accumulator is BN/2 registers).
 //   scheduler   persistent: CTA c takes tiles c, c+P, ... in a banded

@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(NarrowCfg<BN, A_ROWS, KD, S, KSPLIT>::kThreads
                     ok = false;
                     break;
                 }
-                __syncwarp();           // orders lane 0's barrier waits before every lane's reads
+                __syncwarp();
                 tc_fence_after_sync();
                 if (quarter_live) {
                     const uint8_t *slot = sm_scales + sring.i * C::kSlotBytes;
