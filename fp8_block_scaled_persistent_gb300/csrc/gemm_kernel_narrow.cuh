@@ -24,6 +24,9 @@
 //               orders give the same bits) and stores its half.  Every CTA
 //               sends before it waits, so the waits end; nothing goes through
 //               global memory, so no workspace.
+// The library's build (gemm_narrow.cu) runs two K parts of 96-column slices
+// for both A box heights; one part (and 48- or 64-column slices) measured
+// slower and stays a build option.
 // A slice whose width does not divide 128 may straddle one boundary of the
 // 128-column scale blocks: its scale slots then hold both blocks' B scales
 // and each 16-column chunk of the slice takes its block's.  The narrow tile
@@ -46,7 +49,8 @@
 //   warps 2-5   epilogue, one per tensor-memory lane quarter (warp & 3): per
 //               K block tcgen05.ld of its 32 rows x BN columns and
 //               acc += (sa*sb) * P in fp32 registers; the group is released
-//               once its last load has landed.  At the end of a unit, the
+//               once its last load has landed.  Every lane waits and every
+//               lane arrives (warp_wait in ptx.cuh).  At the end of a unit, the
 //               trade of halves (KSPLIT = 2) and bf16 (round to nearest even)
 //               row stores; rows past M and columns past N are not written.
 // With A_ROWS = 64 (M <= 64) only the first 64 rows of A are loaded: the MMA
