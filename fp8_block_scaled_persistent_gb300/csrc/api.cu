@@ -25,9 +25,6 @@ using fp8g::Params;
 
 constexpr int kVersion = 10000;          // 1.0.0
 constexpr int kDefaultSms = 152;
-// the automatic choice runs unsplit problems with at least one 256-row pair
-// tile per resident pair on CTA pairs
-constexpr bool kPairAuto = false;
 constexpr int kMaxDevices = 64;
 constexpr long long kMaxDim = 1ll << 30;  // rows, N and K limits (int32-safe indexing)
 
@@ -471,19 +468,36 @@ bool make_pair_maps(LaunchArgs &a, const void *A, const float *SFA, const void *
 // The pair tile width: the block_n override when one is set, else 256.
 int pair_bn() { return g_override_bn.load() ? g_override_bn.load() : 256; }
 
+// Whether the automatic choice may put the plain GEMM (no addend, not split)
+// on CTA pairs: its 256 x 256 pair tiles must cover no more than an eighth
+// more of the output than the one-CTA kernel's 128 x block_n tiles (M = 384
+// would compute 512 rows for 384).  Measured at 1.9 GHz: 4096 x 7168 x 2048
+// 50.8 -> 49.0 us, 4096 x 24576 x 1536 134.7 -> 127.2 us.  The grouped
+// GEMMs stay on one CTA (contiguous 512 -> 566 us and masked 53.3 -> 58.6 us
+// on pairs: their groups' row blocks fill 256-row tiles less well), and so
+// does a launch with a forced block_n.
+bool pair_auto_ok(int M, int N, int block_n)
+{
+    if (g_override_bn.load() != 0)
+        return false;     // a forced block_n keeps the one-CTA kernel
+    const long long pair_area = (long long)ceil_div(M, 256) * 256 * ceil_div(N, 256) * 256;
+    const long long one_area = (long long)ceil_div(M, 128) * 128 * ceil_div(N, block_n) * block_n;
+    return pair_area * 8 <= one_area * 9;
+}
+
 // Whether an unsplit launch runs on CTA pairs, and over how many pairs.
-// `pair_tiles` is the number of 256 x pair_bn() pair tiles the problem has.
-bool want_pair(long long pair_tiles, const DeviceInfo &dev, int &pairs)
+// `pair_tiles` is the number of 256 x pair_bn() pair tiles the problem has;
+// mode 0 takes pairs when `automatic` allows them and there is at least one
+// pair tile per resident pair.
+bool want_pair(long long pair_tiles, const DeviceInfo &dev, int &pairs, bool automatic)
 {
     const int mode = g_override_pair.load();
-    if (mode < 0 || mode == 2 || pair_tiles <= 0)
+    if (mode < 0 || mode == 2 || pair_tiles <= 0 || (mode == 0 && !automatic))
         return false;
     pairs = fp8g::max_active_pairs(dev.id, pair_bn());
     if (pairs <= 0)
         return false;
-    if (mode > 0)
-        return true;
-    return kPairAuto && pair_tiles >= pairs;
+    return mode > 0 || pair_tiles >= pairs;
 }
 
 // Whether an unsplit launch runs as clusters of two CTAs sharing A over DSMEM
@@ -589,7 +603,8 @@ int run_nt(const void *A, const float *SFA, const void *B, const float *SFB, con
     if (c.split_ctas && !aligned(workspace, 256))
         return FP8G_ERR_MISALIGNED;
     int pairs = 0;
-    if (!c.split_ctas && want_pair((long long)ceil_div(M, 256) * ceil_div(N, pair_bn()), dev, pairs))
+    if (!c.split_ctas && want_pair((long long)ceil_div(M, 256) * ceil_div(N, pair_bn()), dev, pairs,
+                                   C == nullptr && pair_auto_ok(M, N, c.block_n)))
         return run_nt_pair(A, SFA, B, SFB, C, D, M, N, K, pairs, dev, stream);
     if (!c.split_ctas && !C && want_share((long long)ceil_div(M, 128) * share_n_pairs(N), dev, pairs))
         return run_nt_share(A, SFA, B, SFB, D, M, N, K, pairs, dev, stream);
@@ -678,7 +693,7 @@ int fp8_gemm_grouped_contiguous(const void *A, const float *SFA, const void *B, 
     if ((st = current_device_info(dev)) != FP8G_OK)
         return st;
     int pairs = 0;
-    if (want_pair((long long)ceil_div(M_total, 256) * ceil_div(N, pair_bn()), dev, pairs)) {
+    if (want_pair((long long)ceil_div(M_total, 256) * ceil_div(N, pair_bn()), dev, pairs, false)) {
         const int bn = pair_bn();
         LaunchArgs a;
         fill_common(a.p, M_total, N, K, G, SFA, SFB, D, m_indices, bn, dev);
@@ -742,7 +757,7 @@ int fp8_gemm_grouped_masked(const void *A, const float *SFA, const void *B, cons
     if ((st = current_device_info(dev)) != FP8G_OK)
         return st;
     int pairs = 0;
-    if (want_pair((long long)G * ceil_div(M_max, 256) * ceil_div(N, pair_bn()), dev, pairs)) {
+    if (want_pair((long long)G * ceil_div(M_max, 256) * ceil_div(N, pair_bn()), dev, pairs, false)) {
         const int bn = pair_bn();
         LaunchArgs a;
         fill_common(a.p, M_max, N, K, G, SFA, SFB, D, masked_m, bn, dev);
@@ -1013,7 +1028,8 @@ extern "C" int fp8_gemm_nt_noalloc(const void *A, const float *SFA, const void *
             return st;
     }
     int pairs = 0;
-    if (!c.split_ctas && want_pair((long long)ceil_div(M, 256) * ceil_div(N, pair_bn()), dev, pairs))
+    if (!c.split_ctas && want_pair((long long)ceil_div(M, 256) * ceil_div(N, pair_bn()), dev, pairs,
+                                   pair_auto_ok(M, N, c.block_n)))
         return run_nt_pair(A, SFA, B, SFB, nullptr, D, M, N, K, pairs, dev, stream);
     if (!c.split_ctas && want_share((long long)ceil_div(M, 128) * share_n_pairs(N), dev, pairs))
         return run_nt_share(A, SFA, B, SFB, D, M, N, K, pairs, dev, stream);

@@ -213,10 +213,10 @@ int fp8_gemm_set_override(int block_n, int split_ctas);
  * CTA-pair kernel choice (process-wide):
  *   mode  1 : run every unsplit plain, addend, contiguous and masked call on
  *             CTA pairs -- clusters of two CTAs on neighbouring SMs that
- *             share one 256 x 128 output tile through tcgen05.mma.cta_group::2
- *             (each CTA loads its own 128 rows of A and half of the tile's B;
- *             nothing is multicast) -- unless a block_n override other than
- *             128 is set; and every fp8_gemm_nt_ue8m0 call on CTA pairs
+ *             share one 256 x 256 output tile (256 x 128 under a block_n
+ *             override of 128) through tcgen05.mma.cta_group::2 (each CTA
+ *             loads its own 128 rows of A and half of the tile's B; nothing
+ *             is multicast); and every fp8_gemm_nt_ue8m0 call on CTA pairs
  *             sharing 256 x 256 tiles through the block-scaled
  *             tcgen05.mma.cta_group::2 (each CTA holds the scales of its own
  *             rows and of all 256 columns in its tensor memory);
@@ -228,8 +228,14 @@ int fp8_gemm_set_override(int block_n, int split_ctas);
  *             reads A from global memory once.  A block_n override other than
  *             256 turns it off.  Source: TVM TIRx, the "copy_async -> dsmem"
  *             two-CTA shared-to-shared bulk copy;
- *   mode  0 : the automatic choice (the default): one CTA per tile, except
- *             fp8_gemm_nt_ue8m0 with M > 128, which runs on CTA pairs;
+ *   mode  0 : the automatic choice (the default): CTA pairs with 256 x 256
+ *             tiles for an unsplit plain call without addend (fp8_gemm_nt,
+ *             fp8_gemm_nt_noalloc) when no block_n override is set, the
+ *             problem has at least one pair tile per pair the GPU holds at
+ *             once, and the pair tiles cover at most an eighth more of D
+ *             than the one-CTA tiles would (M = 384 stays on one CTA), and
+ *             for fp8_gemm_nt_ue8m0 with M > 128; one CTA per tile for
+ *             everything else;
  *   mode -1 : never use CTA pairs.
  * Results are the same to within fp32 rounding order (bit-identical on
  * exactly representable inputs).  Returns FP8G_ERR_INVALID_ARG for other

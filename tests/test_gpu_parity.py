@@ -254,3 +254,43 @@ def test_full_size_sampled_rows(name):
             check(got[g][rows], ref, f"{name} g{g}")
     again, _, _ = gu.run(p)
     assert np.array_equal(got, again), f"{name}: not deterministic"
+
+
+@pytest.mark.parametrize("M", [384, 1280])
+def test_automatic_pair_choice_padding(M):
+    """The automatic choice leaves a problem on one CTA when 256-row pair
+    tiles would pad M by more than an eighth (384 rows: 512 computed), and
+    takes pairs when they do not (1280 rows); both agree with the oracle on
+    sampled rows, and with the one-CTA kernel (pair mode -1) within the
+    tolerance."""
+    import fp8_block_scaled_persistent_gb300 as fg
+    p = wl.make_nt(M, 24576, 1024, seed=M)
+    got, st, dst = gu.run(p)
+    assert st == 0 and dst == 0
+    rows = gu.sample_rows(p.M, 8, seed=3, must=(0, 127, 128, 255, 256, p.M - 1))
+    ref = oracle.gemm_nt_rows(p.A, p.SFA, p.B, p.SFB, p.M, p.N, p.K, rows, threads=THREADS)
+    check(got[rows], ref, f"automatic {M}")
+    assert fg.fp8_gemm_set_pair_mode(-1) == fg.FP8G_OK
+    try:
+        one, st, dst = gu.run(p)
+    finally:
+        fg.fp8_gemm_set_pair_mode(0)
+    assert st == 0 and dst == 0
+    check(one[rows], ref, f"one CTA {M}")
+
+
+@pytest.mark.parametrize("name", ["dense_4096x7168x2048", "dense_4096x24576x1536"])
+def test_full_size_dense_one_cta(name):
+    """The dense workloads on the one-CTA kernel (pair mode -1; the automatic
+    choice runs them on CTA pairs), sampled rows against the oracle."""
+    import fp8_block_scaled_persistent_gb300 as fg
+    assert fg.fp8_gemm_set_pair_mode(-1) == fg.FP8G_OK
+    try:
+        p = wl.make(name)
+        got, st, dst = gu.run(p)
+    finally:
+        fg.fp8_gemm_set_pair_mode(0)
+    assert st == 0 and dst == 0
+    rows = gu.sample_rows(p.M, 10, seed=4, must=(0, 127, 128, 255, 256, p.M - 1))
+    ref = oracle.gemm_nt_rows(p.A, p.SFA, p.B, p.SFB, p.M, p.N, p.K, rows, threads=THREADS)
+    check(got[rows], ref, f"{name} one CTA")
