@@ -23,10 +23,8 @@
 //     its own bytes with a remote arrive.expect_tx); the leader's one commit
 //     per K block is multicast to the stage's empty barrier in both CTAs,
 //     which frees the stage for both producers and tells both epilogues that
-//     the partial is ready; every lane of the epilogue warps of both CTAs
-//     releases a tensor memory buffer on the leader's barrier (remote
-//     arrive, 2 x 8 x 32 arrivals: 128.7 us rather than 129.1 us on
-//     4096 x 24576 x 1536 against one arrive per warp after a warp sync).
+//     the partial is ready; the epilogue warps of both CTAs release a tensor
+//     memory buffer on the leader's barrier (remote arrive).
 //
 // Roles per CTA are those of the one-CTA kernel (warp 0 producer, warp 1 MMA
 // issuer -- idle in the second CTA --, warps 4-11 epilogue).  Scales are
@@ -93,7 +91,7 @@ struct PairCfg {
 // leader's barrier (a shared::cluster address) once its last load landed.
 template <int COLS, int LD>
 __device__ __forceinline__ void promote_block_pair(float (&acc)[COLS], uint32_t taddr, const float *pa,
-                                                   const float *pb, uint32_t tempty_cluster_addr)
+                                                   const float *pb, uint32_t tempty_cluster_addr, int lane)
 {
     constexpr int NCH = COLS / LD;
     static_assert(COLS % LD == 0, "column split");
@@ -106,10 +104,10 @@ __device__ __forceinline__ void promote_block_pair(float (&acc)[COLS], uint32_t 
             s = *pa * *pb;
         tmem_wait_ld(v);
         if (c + 1 == NCH) {
-            // every lane arrives once its own loads are done (the barrier
-            // counts 32 per warp): no lane waits for the slowest one
             tc_fence_before_sync();
-            mbar_arrive_cluster(tempty_cluster_addr);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_cluster(tempty_cluster_addr);
         }
         fma_cols<LD>(acc + c * LD, v, s);
     }
@@ -280,10 +278,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < NACC; ++i)
-            mbar_init(&tempty[i], 2 * kNumEpiWarps * 32);
+            mbar_init(&tempty[i], 2 * kNumEpiWarps);
         for (int i = 0; i < SR; ++i) {
             mbar_init(&sfull[i], 1);
-            mbar_init(&sempty[i], kNumEpiWarps * 32);
+            mbar_init(&sempty[i], kNumEpiWarps);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -469,11 +467,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
                 // promote, and hand the buffer back to the leader's MMA issuer
                 const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + acc_ring.i * BN + h * COLS;
-                promote_block_pair<COLS, 64>(acc, taddr, pa, pb, leader_tempty + 8u * acc_ring.i);
+                promote_block_pair<COLS, 64>(acc, taddr, pa, pb, leader_tempty + 8u * acc_ring.i, lane);
                 acc_ring.template next<NACC>();
                 ring.template next<S>();
                 if (kc == kScaleChunk - 1 || k + 1 == p.kb) {
-                    mbar_arrive(&sempty[sring.i]);
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&sempty[sring.i]);
                     sring.template next<SR>();
                 }
             }
