@@ -81,7 +81,7 @@ def kernel_of(name):
         return "fp8_gemm_narrow_kernel"
     if name.startswith("ue8m0_"):
         return "fp8_gemm_ue8m0_pair_kernel"
-    if name.startswith("dense_"):
+    if name.startswith("dense_") or name.startswith("acc_"):
         return "fp8_gemm_pair_kernel"
     return "fp8_gemm_kernel"
 

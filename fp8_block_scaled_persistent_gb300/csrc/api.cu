@@ -468,14 +468,15 @@ bool make_pair_maps(LaunchArgs &a, const void *A, const float *SFA, const void *
 // The pair tile width: the block_n override when one is set, else 256.
 int pair_bn() { return g_override_bn.load() ? g_override_bn.load() : 256; }
 
-// Whether the automatic choice may put the plain GEMM (no addend, not split)
-// on CTA pairs: its 256 x 256 pair tiles must cover no more than an eighth
-// more of the output than the one-CTA kernel's 128 x block_n tiles (M = 384
-// would compute 512 rows for 384).  Measured at 1.9 GHz: 4096 x 7168 x 2048
-// 50.8 -> 49.0 us, 4096 x 24576 x 1536 134.7 -> 127.2 us.  The grouped
-// GEMMs stay on one CTA (contiguous 512 -> 566 us and masked 53.3 -> 58.6 us
-// on pairs: their groups' row blocks fill 256-row tiles less well), and so
-// does a launch with a forced block_n.
+// Whether the automatic choice may put the plain GEMM, with or without the
+// addend (not split), on CTA pairs: its 256 x 256 pair tiles must cover no
+// more than an eighth more of the output than the one-CTA kernel's
+// 128 x block_n tiles (M = 384 would compute 512 rows for 384).  Measured at
+// 1.9 GHz: 4096 x 7168 x 2048 50.8 -> 49.0 us, 4096 x 24576 x 1536
+// 134.7 -> 127.2 us, with the addend 65.5 -> 62.1 us.  The grouped GEMMs
+// stay on one CTA (contiguous 512 -> 566 us and masked 53.3 -> 58.6 us on
+// pairs: their groups' row blocks fill 256-row tiles less well), and so does
+// a launch with a forced block_n.
 bool pair_auto_ok(int M, int N, int block_n)
 {
     if (g_override_bn.load() != 0)
@@ -546,6 +547,9 @@ int run_nt_pair(const void *A, const float *SFA, const void *B, const float *SFB
     a.p.num_tiles = a.p.num_m_blocks * a.p.num_n_blocks;
     if (!make_pair_maps(a, A, SFA, B, SFB, D, M, N, M, a.p.kb, a.p.sfa_ld, (long long)a.p.nb * a.p.kb, N, K, bn))
         return FP8G_ERR_CUDA;
+    // 256-column tiles copy the addend through the staging area by TMA
+    if (C && bn == 256 && !make_c_map(&a.tmap_c, C, (uint64_t)M, N))
+        return FP8G_ERR_CUDA;
     a.grid = 2 * std::min(pairs, a.p.num_tiles);
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     return to_status(fp8g::launch_pair(C ? fp8g::kKindNTAcc : fp8g::kKindNT, bn, a));
@@ -604,7 +608,7 @@ int run_nt(const void *A, const float *SFA, const void *B, const float *SFB, con
         return FP8G_ERR_MISALIGNED;
     int pairs = 0;
     if (!c.split_ctas && want_pair((long long)ceil_div(M, 256) * ceil_div(N, pair_bn()), dev, pairs,
-                                   C == nullptr && pair_auto_ok(M, N, c.block_n)))
+                                   pair_auto_ok(M, N, c.block_n)))
         return run_nt_pair(A, SFA, B, SFB, C, D, M, N, K, pairs, dev, stream);
     if (!c.split_ctas && !C && want_share((long long)ceil_div(M, 128) * share_n_pairs(N), dev, pairs))
         return run_nt_share(A, SFA, B, SFB, D, M, N, K, pairs, dev, stream);

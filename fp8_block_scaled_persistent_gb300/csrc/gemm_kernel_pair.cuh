@@ -70,7 +70,7 @@ struct PairCfg {
     static constexpr int kPanelBytes = 32 * kPanelCols * 2;
     static constexpr int kPanelsPerWarp = kColsPerThread / kPanelCols;
     static constexpr int kStagingBytes = kNumEpiWarps * kPanelsPerWarp * kPanelBytes;
-    static constexpr int kBarriers = 2 * kStages + kAccBufs + 2 * kScaleSlots + 1;
+    static constexpr int kBarriers = 2 * kStages + kAccBufs + 2 * kScaleSlots + 4;
     static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + kScaleSlots * kSlotBytes +
                                       kBarriers * 8 + 16 + 1024 /* alignment slack */;
     // registers per thread after reallocation: the epilogue holds BN/2
@@ -240,7 +240,8 @@ template <int BN, int KIND>
 __global__ void __launch_bounds__(kNumThreads, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_sfa,
-                         const __grid_constant__ CUtensorMap tmap_sfb, const __grid_constant__ Params p)
+                         const __grid_constant__ CUtensorMap tmap_sfb, const __grid_constant__ CUtensorMap tmap_c,
+                         const __grid_constant__ Params p)
 {
 #if defined(__CUDA_ARCH__)
     using C = PairCfg<BN>;
@@ -248,6 +249,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     constexpr int NACC = C::kAccBufs;
     constexpr int SR = C::kScaleSlots;
     constexpr int COLS = C::kColsPerThread;
+    // the addend at 256-column tiles: warp 2 copies C into the staging area
+    // and stores the tile, as in the one-CTA kernel (each CTA of the pair
+    // handles the C of its own 128 rows)
+    constexpr bool kHelperC = KIND == kKindNTAcc && BN == 256;
+    static_assert(!kHelperC || (COLS == 2 * kAddendHalfCols &&
+                                C::kPanelsPerWarp * C::kPanelBytes >= 32 * kAddendHalfCols * 4),
+                  "addend halves");
 
     // shared memory, the same layout in both CTAs (the leader's descriptors
     // name the peer's operand tiles by the same offsets):
@@ -265,7 +273,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     uint64_t *sfull = tempty + NACC;   // SR: scale slot landed (local)
     uint64_t *sempty = sfull + SR;     // SR: epilogue finished reading a scale slot (local)
     uint64_t *drain = sempty + SR;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *c_full = drain + 1;      // a half tile of C landed in the staging area (local)
+    uint64_t *c_free = c_full + 1;     // every epilogue warp has added the first half
+    uint64_t *d_ready = c_free + 1;    // every epilogue warp has left its bf16 rows in the staging area
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(d_ready + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -284,6 +295,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_init(&sempty[i], kNumEpiWarps);
         }
         mbar_init(drain, 1);
+        mbar_init(c_full, 1);
+        mbar_init(c_free, kNumEpiWarps);
+        mbar_init(d_ready, kNumEpiWarps);
         *abort_flag = 0;
         fence_mbarrier_init();
         fence_proxy_async_shared();
@@ -294,6 +308,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         prefetch_tensormap(&tmap_d);
         prefetch_tensormap(&tmap_sfa);
         prefetch_tensormap(&tmap_sfb);
+        if (kHelperC)
+            prefetch_tensormap(&tmap_c);
     }
     __syncthreads();
     // both CTAs' barriers are initialised before any remote arrival or copy
@@ -375,6 +391,61 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             for (int i = 0; i < SR; ++i)
                 if (sissued & (1u << i))
                     mbar_wait_drain(&sfull[i], (sissued_parity >> i) & 1u, p.timeout_ns);
+        } else if (kHelperC && warp == 2 && lane == 0) {
+            // ------------------------------------------------ addend/store (accumulate)
+            // Per tile, in this CTA's staging area: once the previous tile's
+            // stores have read it, C's first half (64 of each epilogue warp's
+            // 128 columns, one 3-D box of 4 x 32 rows x 16 fp32 columns per
+            // warp); when every warp has added it, the second half; when
+            // every warp has left its bf16 rows there, the tile's stores.
+            // Rows past M and columns past N arrive as zeros.
+            PairScheduler<KIND> sched(p, false);
+            PairWork w;
+            uint32_t ph = 0, c_issued = 0;
+            bool pending = false, ok = true;
+            while (ok && sched.next(w)) {
+                if (pending)
+                    bulk_wait_group_read<0>();
+                const int chunk0 = (w.n_blk * BN) / 16;     // the tile's first 16-column slab of C
+                for (int rd = 0; rd < 2 && ok; ++rd) {
+                    if (rd == 1 && !mbar_wait(c_free, ph, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(c_full, kNumEpiWarps * C::kPanelsPerWarp * C::kPanelBytes);
+#pragma unroll 1
+                    for (int e = 0; e < kNumEpiWarps; ++e)
+                        tma_load_3d(sm_stage_d + e * C::kPanelsPerWarp * C::kPanelBytes, &tmap_c, c_full, 0,
+                                    w.a_row0 + 32 * (e & 3), chunk0 + (e >> 2) * (COLS / 16) + rd * 4);
+                    ++c_issued;
+                }
+                if (!ok || !mbar_wait(d_ready, ph, ctl)) {
+                    ok = false;
+                    break;
+                }
+                ph ^= 1u;
+#pragma unroll 1
+                for (int e = 0; e < kNumEpiWarps; ++e) {
+                    // the epilogue's rule: full 32-row slabs go by TMA, others
+                    // were written by their warp directly
+                    if (w.valid_rows - 32 * (e & 3) < 32)
+                        continue;
+                    for (int pi = 0; pi < C::kPanelsPerWarp; ++pi) {
+                        const int x = w.n_blk * BN + (e >> 2) * COLS + pi * C::kPanelCols;
+                        if (x < p.N)
+                            tma_store_2d(&tmap_d,
+                                         sm_stage_d + e * C::kPanelsPerWarp * C::kPanelBytes + pi * C::kPanelBytes,
+                                         x, w.a_row0 + 32 * (e & 3));
+                    }
+                }
+                bulk_commit_group();
+                pending = true;
+            }
+            // every store is done and the last addend copy has landed before
+            // the CTA exits
+            bulk_wait_group<0>();
+            if (c_issued)
+                mbar_wait_drain(c_full, (c_issued - 1) & 1u, p.timeout_ns);
         } else if (warp == 1 && lane == 0 && rank == 0) {
             // ------------------------------------------------ MMA issuer (leader)
             PairScheduler<KIND> sched(p, false);
@@ -430,13 +501,37 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         PairWork w;
         Ring ring, acc_ring, sring;
         bool ok = true;
+        uint32_t cph = 0;       // phase of c_full this warp waits for next (addend/store warp)
+        // with the addend/store warp, half 0 of C is added halfway through
+        // the tile's K blocks, which releases the staging area for half 1;
+        // below 8 K blocks both halves are added after the loop.  Measured on
+        // 4096 x 7168 x 2048 (16 K blocks), adding half 0 after K block 4,
+        // 6, 8, 10, 11 or 12: 66.0, 62.7, 62.1, 62.1, 62.8, 65.0 us
+        const bool c_early = p.kb >= 8;
+        const int k_c0 = p.kb / 2;
+        // wait for half rd of C, add it and, for the first half, hand the
+        // staging area back
+        auto take_c = [&](float (&a)[COLS], int rd) -> bool {
+            if (!warp_wait(c_full, cph, ctl))
+                return false;
+            cph ^= 1u;
+            __syncwarp();
+            add_c_box<COLS>(a, panels, lane, rd);
+            __syncwarp();           // every lane's reads before the area is reused
+            if (rd == 0 && lane == 0)
+                mbar_arrive(c_free);
+            return true;
+        };
+        (void)take_c;
+        (void)c_early;
+        (void)k_c0;
         while (ok && sched.next(w)) {
             float acc[COLS];
             if (KIND == kKindNTAcc && !bounds_ok(w.a_row0 + w.valid_rows <= p.rows || w.valid_rows == 0, ctl)) {
                 ok = false;
                 break;
             }
-            if constexpr (KIND == kKindNTAcc) {
+            if constexpr (KIND == kKindNTAcc && !kHelperC) {
                 // the addend starts the accumulator (the only CTA of the tile)
                 Work w1;
                 w1.a_row0 = w.a_row0;
@@ -476,6 +571,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         mbar_arrive(&sempty[sring.i]);
                     sring.template next<SR>();
                 }
+                if constexpr (kHelperC) {
+                    if (c_early && k == k_c0 && !take_c(acc, 0)) {
+                        ok = false;
+                        break;
+                    }
+                }
             }
             if (!ok)
                 break;
@@ -486,17 +587,34 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (rows_ok > 0 && !bounds_ok(y_row0 >= 0 && y_row0 + rows_ok <= p.d_rows_total, ctl))
                 rows_ok = 0;
             const int x = w.n_blk * BN + h * COLS;
-            // the previous tile's store has had a whole tile to read this
-            // warp's panel; make sure it has
-            if (lane == 0)
-                bulk_wait_group_read<0>();
-            __syncwarp();
+            if constexpr (kHelperC) {
+                // the addend/store warp waited for the previous tile's stores
+                // before copying C here; the second half (and, for short K,
+                // the first) goes in now
+                if ((!c_early && !take_c(acc, 0)) || !take_c(acc, 1)) {
+                    ok = false;
+                    break;
+                }
+            } else {
+                // the previous tile's store has had a whole tile to read this
+                // warp's panel; make sure it has
+                if (lane == 0)
+                    bulk_wait_group_read<0>();
+                __syncwarp();
+            }
             constexpr int PC = C::kPanelCols;
 #pragma unroll
             for (int pi = 0; pi < COLS / PC; ++pi)
                 if (x + pi * PC < p.N && rows_ok > 0)
-                    store_panel<PC, false>(acc + pi * PC, panels + pi * C::kPanelBytes, &tmap_d, p, x + pi * PC,
-                                           y_row0, rows_ok, lane);
+                    store_panel<PC, false, !kHelperC>(acc + pi * PC, panels + pi * C::kPanelBytes, &tmap_d, p,
+                                                      x + pi * PC, y_row0, rows_ok, lane);
+            if constexpr (kHelperC) {
+                // the full 32-row slabs are in the staging area: the
+                // addend/store warp stores them
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(d_ready);
+            }
         }
         if constexpr (KIND == kKindNTAcc)
             cp_async_wait_all();

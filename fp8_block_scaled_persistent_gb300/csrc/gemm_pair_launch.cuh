@@ -54,7 +54,7 @@ cudaError_t pair_launch_one(const LaunchArgs &a)
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, fp8_gemm_pair_kernel<BN, KIND>, a.tmap_a, a.tmap_b, a.tmap_d, a.tmap_sfa,
-                              a.tmap_sfb, a.p);
+                              a.tmap_sfb, a.tmap_c, a.p);
 }
 
 template <int BN>

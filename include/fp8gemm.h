@@ -229,8 +229,9 @@ int fp8_gemm_set_override(int block_n, int split_ctas);
  *             256 turns it off.  Source: TVM TIRx, the "copy_async -> dsmem"
  *             two-CTA shared-to-shared bulk copy;
  *   mode  0 : the automatic choice (the default): CTA pairs with 256 x 256
- *             tiles for an unsplit plain call without addend (fp8_gemm_nt,
- *             fp8_gemm_nt_noalloc) when no block_n override is set, the
+ *             tiles for an unsplit plain call, with or without the addend
+ *             (fp8_gemm_nt, fp8_gemm_nt_noalloc, fp8_gemm_nt_accumulate),
+ *             when no block_n override is set, the
  *             problem has at least one pair tile per pair the GPU holds at
  *             once, and the pair tiles cover at most an eighth more of D
  *             than the one-CTA tiles would (M = 384 stays on one CTA), and

@@ -138,3 +138,34 @@ def test_full_size_sampled_rows():
     check(got[rows], _ref(p, rows), p.name)
     again, _, _ = gu.run(p)
     assert np.array_equal(got, again), "not deterministic"
+
+
+def test_full_size_one_cta():
+    """The full-size workload on the one-CTA kernel (pair mode -1; the
+    automatic choice runs it on CTA pairs), sampled rows against the oracle."""
+    import fp8_block_scaled_persistent_gb300 as fg
+    assert fg.fp8_gemm_set_pair_mode(-1) == fg.FP8G_OK
+    try:
+        p = wl.make("acc_4096x7168x2048")
+        got, st, dst = gu.run(p)
+    finally:
+        fg.fp8_gemm_set_pair_mode(0)
+    assert st == 0 and dst == 0
+    rows = gu.sample_rows(p.M, 10, seed=5, must=(0, 127, 128, 255, 256, p.M - 1))
+    check(got[rows], _ref(p, rows), f"{p.name} one CTA")
+
+
+def test_pair_addend_ragged_edges():
+    """The addend on CTA pairs with 256-column tiles (the addend/store warp
+    copies C through the staging area), forced by pair mode 1: ragged M and
+    N, a pair whose second CTA has no rows, K below and above 8 blocks."""
+    import fp8_block_scaled_persistent_gb300 as fg
+    assert fg.fp8_gemm_set_pair_mode(1) == fg.FP8G_OK
+    try:
+        for (M, N, K) in [(100, 272, 640), (300, 528, 1024), (513, 256, 2304), (256, 784, 1280)]:
+            p = wl.make_nt_acc(M, N, K, seed=M + N + K)
+            got, st, dst = gu.run(p)
+            assert st == 0 and dst == 0
+            check(got, _ref(p), f"pair acc {M}x{N}x{K}")
+    finally:
+        fg.fp8_gemm_set_pair_mode(0)
