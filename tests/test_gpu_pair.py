@@ -7,8 +7,9 @@ or no rows, column tails), exact small-integer inputs bit for bit, the
 contiguous layout with pair tiles whose two 128-row blocks belong to
 different groups (the second pass), skipped and out-of-range blocks, the
 masked layout with counts on both sides of 128 and 256 (rows past a count
-untouched), the fp32 addend, guard bands, determinism, a CUDA graph replay,
-and the full-size workloads on sampled rows.
+untouched), the fp32 addend (at 256-column tiles copied through the staging
+area by the addend/store warp), guard bands, determinism, a CUDA graph
+replay, and the full-size workloads on sampled rows.
 """
 import numpy as np
 import pytest
@@ -155,7 +156,7 @@ def test_pair_graph_replay_bit_identical():
     import torch
     import fp8_block_scaled_persistent_gb300 as fg
     probs = [wl.make_nt(512, 1024, 1024, seed=41), wl.make_masked([5, 200, 0], 256, 256, 512, seed=43),
-             wl.make_contiguous([128, 256], 256, 512, seed=44)]
+             wl.make_contiguous([128, 256], 256, 512, seed=44), wl.make_nt_acc(300, 528, 1280, seed=45)]
     tens = [gu.dev_tensors(p) for p in probs]
     side = torch.cuda.Stream()
     ref = [gu.new_d(p) for p in probs]
@@ -180,7 +181,7 @@ def test_pair_graph_replay_bit_identical():
 
 
 FULL = ["dense_4096x7168x2048", "dense_4096x24576x1536", "contiguous_g8_n4096_k7168",
-        "masked_g16_m256_n7168_k2048"]
+        "masked_g16_m256_n7168_k2048", "acc_4096x7168x2048"]
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -191,6 +192,10 @@ def test_pair_full_size_sampled_rows(name):
     if p.kind == "nt":
         rows = gu.sample_rows(p.M, 12, seed=1, must=(0, 127, 128, 255, 256, p.M - 1))
         ref = oracle.gemm_nt_rows(p.A, p.SFA, p.B, p.SFB, p.M, p.N, p.K, rows, threads=THREADS)
+        check(got[rows], ref, name)
+    elif p.kind == "nt_acc":
+        rows = gu.sample_rows(p.M, 12, seed=1, must=(0, 127, 128, 255, 256, p.M - 1))
+        ref = oracle.gemm_nt_acc_rows(p.A, p.SFA, p.B, p.SFB, p.C, p.M, p.N, p.K, rows, threads=THREADS)
         check(got[rows], ref, name)
     elif p.kind == "contiguous":
         starts = np.cumsum([0] + p.meta["group_rows"][:-1])
