@@ -27,9 +27,12 @@
 //     memory buffer on the leader's barrier (remote arrive).
 //
 // Roles per CTA are those of the one-CTA kernel (warp 0 producer, warp 1 MMA
-// issuer -- idle in the second CTA --, warps 4-11 epilogue).  Scales are
-// per CTA: each loads the A scales of its own rows and the B scales of the
-// tile's 128 columns into its own scale ring.
+// issuer -- idle in the second CTA --, warps 4-11 epilogue; with the fp32
+// addend at BN = 256, warp 2 copies each tile's C of the CTA's own 128 rows
+// into the staging area in two halves and stores the bf16 tile, as the
+// one-CTA kernel's addend/store warp does).  Scales are per CTA: each loads
+// the A scales of its own rows and the B scales of the tile's 128 columns
+// into its own scale ring.
 //
 // Every wait is bounded.  A wait that runs out raises the abort flag of both
 // CTAs; both then drain and meet at the final cluster barrier, after which
